@@ -1,0 +1,189 @@
+/*
+ * wenc.h -- C ABI of libwenc.so: the Whisper encoder's pre-LayerNorm transformer
+ * blocks, GPU-resident on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the encoder block of the three pages this library follows:
+ *   "inferencelayer 0.2.4 src/whisper_gpu.rs" (WhisperEncoderGpu::forward, the
+ *     VANILLA_ATTN and LN_SRC shaders),
+ *   "turbospark-runtime 0.3.0 src/whisper/metal.rs" (EncLayerGpu, encode_partial,
+ *     encode_layer),
+ *   "oxinfer 0.0.5 src/whisper/model.rs" (WhisperModel::encode, make_lin, Precision).
+ * Per block:  x += Wo . Attn(LN1(x) Wq^T + bq, LN1(x) Wk^T, LN1(x) Wv^T + bv) + bo
+ *             x += W2 . GELU_erf(LN2(x) W1^T + b1) + b2
+ * then, optionally, a final LayerNorm. Attention is non-causal scaled-dot attention
+ * (scale hd^-0.5) over the whole window, with no mask and no positional term.
+ *
+ * Conventions for every entry point:
+ *  - All pointers are DEVICE pointers unless stated otherwise; sizes are element counts.
+ *  - Activations are row-major [rows, width]; a window of T frames occupies T consecutive
+ *    rows; head h of an attention operand sits in columns h*hd .. h*hd+hd-1.
+ *  - Weight matrices are [n_out, n_in] row-major (PyTorch layout); y = x W^T + b.
+ *  - bf16 buffers are raw bfloat16 bit patterns (uint16_t).
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *    Entry points marked "stream-ordered" do not synchronise the host and allocate nothing.
+ *  - Argument errors are reported synchronously as a status; the message is available
+ *    from wenc_last_error() on the same host thread. Nothing aborts the process.
+ *  - Device-side waits are bounded (about one second); a wait that runs out records
+ *    WENC_ERR_DEVICE_TIMEOUT in a device error word instead of hanging the GPU. It is
+ *    reported by wenc_sync_status() and by the next wenc_forward* call on that handle.
+ */
+#ifndef WENC_H
+#define WENC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define WENC_API __attribute__((visibility("default")))
+#else
+#define WENC_API
+#endif
+
+typedef struct CUstream_st* wenc_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  WENC_OK = 0,
+  WENC_ERR_INVALID_ARG = 1,     /* null pointer, bad size, misaligned buffer */
+  WENC_ERR_UNSUPPORTED = 2,     /* a shape or mode this build does not implement (e.g. hd != 64) */
+  WENC_ERR_OOM = 3,             /* device allocation failed (wenc_create only) */
+  WENC_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed; see wenc_last_error() */
+  WENC_ERR_DEVICE_TIMEOUT = 5   /* a bounded device-side wait ran out (pipeline stalled) */
+} wenc_status;
+
+/* Storage type of the weight matrices handed to wenc_create. Norm parameters and
+ * biases are always float32 ("Norms, biases and positions always stay f32",
+ * oxinfer src/whisper/model.rs, Precision). */
+typedef enum { WENC_DTYPE_F32 = 0, WENC_DTYPE_BF16 = 1 } wenc_dtype;
+
+/* Arithmetic of the contractions. BF16: bf16 operands on the tensor cores with fp32
+ * accumulation; LayerNorm statistics, softmax, GELU and the residual stream are fp32. */
+typedef enum { WENC_PREC_BF16 = 0 } wenc_precision;
+
+/* Epilogues of wenc_linear (the fused forms the block uses). */
+typedef enum {
+  WENC_EPI_BIAS_BF16 = 0,       /* out(bf16) = A W^T + bias                         (QKV)   */
+  WENC_EPI_BIAS_GELU_BF16 = 1,  /* out(bf16) = GELU_erf(A W^T + bias)               (fc1)   */
+  WENC_EPI_BIAS_RESID_F32 = 2   /* out(f32)  = resid + A W^T + bias (resid may == out) (out-proj, fc2) */
+} wenc_epilogue;
+
+typedef struct {
+  int n_layers;      /* >= 1 */
+  int d_model;       /* = n_heads * head_dim; a multiple of 128 (384, 512, 768, 1280, ...) */
+  int n_heads;       /* >= 1 */
+  int head_dim;      /* must be 64 */
+  int ffn_dim;       /* a multiple of 128 */
+  int seq_len;       /* frames per window, 1..4096 (1500 for Whisper's 30 s window) */
+  int max_batch;     /* windows per call, >= 1; sizes the workspace */
+  int final_ln;      /* nonzero: apply the final LayerNorm after the last block */
+  float ln_eps;      /* LayerNorm epsilon (1e-5 on all three pages) */
+  int weight_dtype;  /* wenc_dtype of the matrices in wenc_layer_weights */
+  int precision;     /* wenc_precision; only WENC_PREC_BF16 */
+} wenc_config;
+
+/* One block's parameters, as DEVICE pointers owned by the caller. Matrices are
+ * [n_out, n_in] row-major in config.weight_dtype: wq, wk, wv, wo [d, d]; w1 [f, d];
+ * w2 [d, f]. Vectors are float32: ln*_w, ln*_b, bq, bv, bo [d]; b1 [f]; b2 [d].
+ * bk must be NULL: the K projection has no bias (turbospark-runtime EncLayerGpu). */
+typedef struct {
+  const float* ln1_w; const float* ln1_b;
+  const void* wq; const float* bq;
+  const void* wk; const float* bk;
+  const void* wv; const float* bv;
+  const void* wo; const float* bo;
+  const float* ln2_w; const float* ln2_b;
+  const void* w1; const float* b1;
+  const void* w2; const float* b2;
+} wenc_layer_weights;
+
+typedef struct wenc wenc; /* opaque handle */
+
+/* wenc_create -- validate `cfg`, pack the weights into library-owned device memory
+ * (matrices rounded to bf16, nearest-even, as oxinfer make_lin does for Precision::Bf16;
+ * Q/K/V packed into one [3d, d] matrix with a [3d] bias whose K slot is zero, the
+ * layout of turbospark-runtime DecLayerGpu::self_qkv_w), and allocate the activation
+ * workspace for cfg->max_batch windows (all scratch sized once, as turbospark-runtime's
+ * engine does at open). `layers` holds cfg->n_layers entries; lnf_w/lnf_b [d] are read
+ * only when cfg->final_ln is set (may be NULL otherwise). The caller's buffers may be
+ * freed once this returns: it synchronises `stream` before returning.
+ * Errors: INVALID_ARG (null/inconsistent sizes, bk != NULL), UNSUPPORTED (hd != 64,
+ * d or f not a multiple of 128, seq_len > 4096), OOM, CUDA. On error *out is NULL. */
+WENC_API wenc_status wenc_create(const wenc_config* cfg, const wenc_layer_weights* layers,
+                        const float* lnf_w, const float* lnf_b, wenc_stream_t stream,
+                        wenc** out);
+
+/* wenc_forward -- hidden_out = Encoder(hidden_in), both float32 [B, seq_len, d_model],
+ * caller-owned, hidden_in == hidden_out allowed. 1 <= B <= max_batch. Stream-ordered.
+ * One call runs every block and, if configured, the final LayerNorm
+ * (inferencelayer WhisperEncoderGpu::forward; oxinfer WhisperModel::encode). */
+WENC_API wenc_status wenc_forward(wenc* h, const float* hidden_in, float* hidden_out, int B,
+                         wenc_stream_t stream);
+
+/* wenc_forward_layers -- run blocks first .. first+count-1 only, then the final
+ * LayerNorm iff apply_final_ln (and the handle has one). The per-layer bisection of
+ * turbospark-runtime encode_partial(stop_after). Same buffers and rules as wenc_forward;
+ * count may be 0 (then only the final LN, or a copy, runs). Stream-ordered. */
+WENC_API wenc_status wenc_forward_layers(wenc* h, const float* hidden_in, float* hidden_out, int B,
+                                int first, int count, int apply_final_ln, wenc_stream_t stream);
+
+/* wenc_forward_launches -- number of kernel launches one wenc_forward_layers call with
+ * these arguments makes (for launch accounting). Returns -1 on bad arguments. */
+WENC_API int wenc_forward_launches(const wenc* h, int first, int count, int apply_final_ln);
+
+/* wenc_set_launch_events -- optional timing hook. When `events` is non-NULL, the next
+ * forward call records events[0] before its first launch and events[i+1] after launch i
+ * (each a cudaEvent_t created by the caller), for n_events >= launches + 1; the hook
+ * then clears itself. kinds (may be NULL) receives, per launch, 0 = LayerNorm,
+ * 1 = QKV GEMM, 2 = attention, 3 = out-proj GEMM, 4 = fc1 GEMM, 5 = fc2 GEMM,
+ * 6 = final LayerNorm, 7 = copy. */
+WENC_API wenc_status wenc_set_launch_events(wenc* h, void* const* events, int n_events, int* kinds);
+
+/* wenc_attention -- out = softmax(q k^T * hd^-0.5) v per (window, head), non-causal,
+ * over all T keys of each window (inferencelayer VANILLA_ATTN; turbospark-runtime
+ * encode_layer's per-head score planes, row softmax and PV).
+ * q, k, v, out: bf16 [B, T, H, hd] contiguous (row stride H*hd), caller-owned; the
+ * softmax and accumulation are fp32, the output rounded to bf16. hd must be 64;
+ * 1 <= T <= 1<<20; B, H >= 1. Buffers must be 16-byte aligned. Stream-ordered.
+ * A stalled device wait is recorded in the library's global error word
+ * (see wenc_sync_status(NULL)). */
+WENC_API wenc_status wenc_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                           uint16_t* out, int B, int T, int H, int hd, wenc_stream_t stream);
+
+/* wenc_layernorm -- y = (x - mean) / sqrt(var + eps) * w + b per row of x float32
+ * [rows, d] (biased variance; inferencelayer LN_SRC). y is bf16 when out_bf16 != 0 (the
+ * cast that feeds the next GEMM), else float32. d a multiple of 128, <= 2048. Stream-ordered. */
+WENC_API wenc_status wenc_layernorm(const float* x, const float* w, const float* b, void* y, int rows,
+                           int d, float eps, int out_bf16, wenc_stream_t stream);
+
+/* wenc_linear -- one contraction of the block with a fused epilogue (see wenc_epilogue):
+ * A bf16 [M, K], W bf16 [N, K] (K-major, PyTorch layout), bias float32 [N], resid/out
+ * [M, N] (bf16 or f32 per the epilogue). N a multiple of 128, K a multiple of 64, M >= 1.
+ * Buffers 16-byte aligned. Stream-ordered. The matmul_bias
+ * step of turbospark-runtime encode_layer with its add / gelu_erf passes fused in. */
+WENC_API wenc_status wenc_linear(const uint16_t* A, const uint16_t* W, const float* bias,
+                        const float* resid, void* out, int M, int N, int K, int epilogue,
+                        wenc_stream_t stream);
+
+/* wenc_sync_status -- synchronise the device and read the device error word of `h`
+ * (or, when h is NULL, the word shared by the handle-less entry points), clearing it.
+ * Returns WENC_OK, WENC_ERR_DEVICE_TIMEOUT or WENC_ERR_CUDA. */
+WENC_API wenc_status wenc_sync_status(wenc* h);
+
+/* wenc_destroy -- free everything the handle owns (synchronises the device first).
+ * NULL is a no-op. */
+WENC_API void wenc_destroy(wenc* h);
+
+/* wenc_last_error -- message for the last non-OK status returned on this host thread
+ * ("" if none). The pointer stays valid until the next call on this thread. */
+WENC_API const char* wenc_last_error(void);
+
+/* wenc_version -- "wenc <major>.<minor> sm_103a". */
+WENC_API const char* wenc_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* WENC_H */

@@ -1,0 +1,163 @@
+"""Block and stack parity of wenc_forward / wenc_forward_layers against the f64 oracle.
+
+Gates (the bf16 tensor-core bar): per block, max|err| <= 2e-2 x RMS and cosine >= 0.9999 on
+the block output; the block's update y - x is gated too (2e-2 x RMS(y - x), cosine >= 0.999),
+because the attention branch is small next to the residual and a wrong attention kernel
+would otherwise hide under it. Per-block mode feeds block i the GPU's own output of block
+i-1 (the bisection of turbospark-runtime encode_partial), so error does not compound.
+Large stacks are checked on sampled rows of the first and last window: LN1, K and V run
+over the whole window, the rest for the sampled rows only (exact for those rows).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import gate, make_encoder
+
+pytestmark = pytest.mark.gpu
+
+
+def _t(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _block_gates(x_in, y_gpu, y_ref, what):
+    gate(y_gpu, y_ref, what=f"{what} output")
+    gate(y_gpu - x_in, y_ref - x_in, cos_min=0.999, what=f"{what} update")
+
+
+def test_tiny_block_full():
+    """One block, tiny dims, f32 weights (rounded to bf16 by the library), whole window."""
+    import torch
+    w = synth.WORKLOADS["tiny_block"]
+    enc, layers, _, rng = make_encoder(w)
+    x = synth.make_input(w, rng)
+    y = enc.forward(_t(x))
+    torch.cuda.synchronize()
+    enc.sync_status()
+    x1_ref, y_ref = oracle.encoder_block(x, layers[0], w.n_heads, return_mid=True)
+    _block_gates(x.astype(np.float64), y.cpu().numpy(), y_ref, "tiny block")
+
+
+def test_tiny_block_attention_branch_via_steps():
+    """The attention half of the tiny block through the step entry points: x1 - x vs the oracle."""
+    import torch
+    from transformer_encoder_gb300 import attention, layernorm, linear
+    w = synth.WORKLOADS["tiny_block"]
+    _, layers, _, rng = make_encoder(w)
+    p = layers[0]
+    x = synth.make_input(w, rng)[0]
+    d, H = w.d_model, w.n_heads
+    xn = layernorm(_t(x), _t(p["ln1_w"]), _t(p["ln1_b"]))
+    wqkv = _t(np.concatenate([p["wq"], p["wk"], p["wv"]])).to(torch.bfloat16)
+    bqkv = _t(np.concatenate([p["bq"], np.zeros(d, np.float32), p["bv"]]))
+    qkv = linear(xn, wqkv, bqkv, 0)
+    q, k, v = (qkv[:, i * d:(i + 1) * d].contiguous().view(1, w.seq_len, H, 64) for i in range(3))
+    o = attention(q, k, v).view(w.seq_len, d)
+    x1 = linear(o, _t(p["wo"]).to(torch.bfloat16), _t(p["bo"]), 2, resid=_t(x))
+    torch.cuda.synchronize()
+    x1_ref, _ = oracle.encoder_block(x, p, H, return_mid=True)
+    gate(x1.cpu().numpy() - x, x1_ref - x, cos_min=0.999, what="attention branch")
+
+
+def _per_block(w, enc, layers, final, x, full: bool):
+    """Run block by block on the GPU; compare each block (all rows or sampled rows)."""
+    import torch
+    cur = _t(x)
+    B = w.batch
+    sample = np.unique(np.r_[0, 1, 127, 128, 1407, 1408, w.seq_len - 1,
+                             np.random.default_rng(0).integers(0, w.seq_len, 121)])
+    for i, p in enumerate(layers):
+        nxt = enc.forward_layers(cur, first=i, count=1, final_ln=False)
+        torch.cuda.synchronize()
+        x_in = cur.cpu().numpy().astype(np.float64)
+        y = nxt.cpu().numpy()
+        if full:
+            y_ref = oracle.encoder_block(x_in, p, w.n_heads)
+            _block_gates(x_in, y, y_ref, f"{w.name} block {i}")
+        else:
+            for b in sorted({0, B - 1}):
+                _, y_ref = oracle.block_rows(x_in[b], sample, p, w.n_heads)
+                _block_gates(x_in[b, sample], y[b, sample], y_ref, f"{w.name} block {i} window {b}")
+        cur = nxt
+    if final is not None:
+        out = enc.forward_layers(cur, first=len(layers), count=0, final_ln=True)
+        torch.cuda.synchronize()
+        ref = oracle.layer_norm(cur.cpu().numpy(), final[0], final[1])
+        gate(out.cpu().numpy(), ref, what=f"{w.name} final LN")
+    return cur
+
+
+def test_tiny_stack_per_block_and_whole():
+    import torch
+    w = synth.WORKLOADS["tiny_stack"]
+    enc, layers, final, rng = make_encoder(w)
+    x = synth.make_input(w, rng)
+    last = _per_block(w, enc, layers, final, x, full=True)
+    y = enc.forward(_t(x))
+    torch.cuda.synchronize()
+    # whole stack vs the oracle run end to end (errors compound over 4 blocks; same gate)
+    gate(y.cpu().numpy(), oracle.encoder_stack(x, layers, w.n_heads, final=final), what="tiny stack end to end")
+    # wenc_forward is exactly the per-block chain plus the final LN
+    chained = enc.forward_layers(last, first=w.n_layers, count=0, final_ln=True)
+    torch.cuda.synchronize()
+    assert torch.equal(y, chained)
+
+
+def test_base_stack_per_block_full():
+    w = synth.WORKLOADS["base_stack"]
+    enc, layers, final, rng = make_encoder(w)
+    _per_block(w, enc, layers, final, synth.make_input(w, rng), full=True)
+
+
+def test_small_stack_per_block_sampled():
+    w = synth.WORKLOADS["small_stack"]
+    enc, layers, final, rng = make_encoder(w)
+    _per_block(w, enc, layers, final, synth.make_input(w, rng), full=False)
+
+
+def test_large_stack_per_block_sampled():
+    """Large-v3 dims, batch 16, 32 blocks: the launch configuration the bench times."""
+    import torch
+    w = synth.WORKLOADS["large_stack"]
+    enc, layers, final, rng = make_encoder(w)
+    x = synth.make_input(w, rng)
+    last = _per_block(w, enc, layers, final, x, full=False)
+    y = enc.forward(_t(x))
+    chained = enc.forward_layers(last, first=w.n_layers, count=0, final_ln=True)
+    torch.cuda.synchronize()
+    assert torch.equal(y, chained)
+
+
+def test_forward_in_place_and_partial_batch():
+    import torch
+    w = synth.WORKLOADS["tiny_stack"]
+    enc, layers, final, rng = make_encoder(w, max_batch=3)
+    x = np.concatenate([synth.make_input(w, rng, batch=3)])
+    ref = enc.forward(_t(x))
+    one = enc.forward(_t(x[1:2]))          # B < max_batch
+    buf = _t(x)
+    enc.forward(buf, out=buf)              # in place
+    torch.cuda.synchronize()
+    assert torch.equal(buf, ref)
+    assert torch.equal(one[0], ref[1])     # windows are independent
+    assert torch.equal(enc.forward(_t(x)), ref)  # deterministic
+
+
+def test_argument_errors():
+    import torch
+    from transformer_encoder_gb300 import WencError
+    w = synth.WORKLOADS["tiny_block"]
+    enc, _, _, rng = make_encoder(w)
+    x = _t(synth.make_input(w, rng))
+    with pytest.raises(WencError, match="INVALID_ARG"):
+        enc.forward(torch.cat([x, x]))  # B = 2 > max_batch = 1
+    with pytest.raises(WencError, match="INVALID_ARG"):
+        enc.forward_layers(x, first=1, count=1)
+    with pytest.raises(WencError, match="UNSUPPORTED"):
+        from transformer_encoder_gb300 import attention
+        q = torch.zeros(1, 8, 2, 32, dtype=torch.bfloat16, device="cuda")
+        attention(q, q, q)
+    enc.sync_status()

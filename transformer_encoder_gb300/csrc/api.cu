@@ -1,0 +1,599 @@
+// api.cu -- the C ABI of libwenc.so: argument checking, weight packing, workspace,
+// tensor maps and the per-block launch sequence. Every step of the computation runs in
+// the kernels of ln.cu, gemm.cu and attn.cu; this file only prepares and orders them.
+//
+// Block order (turbospark-runtime 0.3.0 src/whisper/metal.rs, encode_layer; inferencelayer
+// 0.2.4 src/whisper_gpu.rs, WhisperEncoderGpu::forward; oxinfer 0.0.5 src/whisper/model.rs,
+// WhisperModel::encode), with each add/activation folded into the producing kernel:
+//   LN1(x) -> xn (bf16) ; QKV = xn Wqkv^T + [bq;0;bv] ; o = Attn(QKV)
+//   x = x + o Wo^T + bo ; LN2(x) -> xn ; u = GELU(xn W1^T + b1) ; x = x + u W2^T + b2
+// and the final LayerNorm into the caller's output.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "launch.h"
+#include "wenc.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+wenc_status fail(wenc_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+wenc_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(WENC_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool is_device_accessible(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+// ---------------------------------------------------------------- tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    cudaGetLastError();
+  });
+  return fn;
+}
+
+// Device error word shared by the handle-less entry points.
+__device__ uint32_t g_device_error_word;
+
+uint32_t* global_error_word(std::string* why) {
+  static uint32_t* addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    *why = "no current CUDA device";
+    return nullptr;
+  }
+  if (!addr[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_device_error_word);
+    if (e != cudaSuccess) {
+      *why = std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e);
+      return nullptr;
+    }
+    addr[dev] = static_cast<uint32_t*>(p);
+  }
+  return addr[dev];
+}
+
+bool device_is_sm103(std::string* why) {
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    *why = "no CUDA device";
+    return false;
+  }
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3) {
+    char b[128];
+    snprintf(b, sizeof(b), "device %d is sm_%d%d; this library is built for sm_103a only", dev, major, minor);
+    *why = b;
+    return false;
+  }
+  return true;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+}  // namespace
+
+namespace wenc_host {
+
+bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
+                       uint32_t box_inner, uint32_t box_outer, std::string* why) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) {
+    *why = "cuTensorMapEncodeTiled is not available from the driver";
+    return false;
+  }
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_stride_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char b[160];
+    snprintf(b, sizeof(b), "cuTensorMapEncodeTiled(2d %llu x %llu) failed with %d", (unsigned long long)inner,
+             (unsigned long long)outer, static_cast<int>(r));
+    *why = b;
+    return false;
+  }
+  return true;
+}
+
+bool make_tmap_3d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t dim1, uint64_t dim2,
+                       uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box_inner, uint32_t box1,
+                       std::string* why) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) {
+    *why = "cuTensorMapEncodeTiled is not available from the driver";
+    return false;
+  }
+  cuuint64_t dims[3] = {inner, dim1, dim2};
+  cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  cuuint32_t box[3] = {box_inner, box1, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char b[160];
+    snprintf(b, sizeof(b), "cuTensorMapEncodeTiled(3d) failed with %d", static_cast<int>(r));
+    *why = b;
+    return false;
+  }
+  return true;
+}
+
+}  // namespace wenc_host
+
+// ================================================================ the handle
+struct wenc {
+  wenc_config cfg;
+  int device = 0;
+  int num_sms = 1;
+  struct Layer {
+    uint16_t *wqkv, *wo, *w1, *w2;  // bf16, [n_out, n_in]
+    float *ln1_w, *ln1_b, *bqkv, *bo, *ln2_w, *ln2_b, *b1, *b2;
+    CUtensorMap tm_wqkv, tm_wo, tm_w1, tm_w2;
+  };
+  std::vector<Layer> layers;
+  float* lnf_w = nullptr;
+  float* lnf_b = nullptr;
+  int bn_qkv = 0, bn_o = 0, bn_1 = 0, bn_2 = 0;
+  // workspace (rows = max_batch * seq_len)
+  float* x = nullptr;
+  uint16_t *xn = nullptr, *qkv = nullptr, *o = nullptr, *u = nullptr;
+  CUtensorMap tm_xn, tm_o, tm_u, tm_q, tm_kv;
+  void* weight_arena = nullptr;
+  void* work_arena = nullptr;
+  uint32_t* err_host = nullptr;  // mapped pinned word: the device writes, the host reads without a sync
+  uint32_t* err_dev = nullptr;
+  // timing hook (one call)
+  std::vector<cudaEvent_t> events;
+  int* kinds = nullptr;
+};
+
+namespace {
+
+struct Arena {
+  size_t used = 0;
+  size_t take(size_t bytes) {
+    size_t off = used;
+    used += (bytes + 255) & ~size_t(255);
+    return off;
+  }
+};
+
+wenc_status check_config(const wenc_config* c) {
+  if (!c) return fail(WENC_ERR_INVALID_ARG, "config is NULL");
+  if (c->n_layers < 1) return fail(WENC_ERR_INVALID_ARG, "n_layers must be >= 1 (got %d)", c->n_layers);
+  if (c->n_heads < 1 || c->head_dim < 1 || c->d_model < 1 || c->ffn_dim < 1 || c->seq_len < 1 || c->max_batch < 1)
+    return fail(WENC_ERR_INVALID_ARG, "sizes must be positive");
+  if (c->d_model != c->n_heads * c->head_dim)
+    return fail(WENC_ERR_INVALID_ARG, "d_model %d != n_heads %d * head_dim %d", c->d_model, c->n_heads, c->head_dim);
+  if (c->head_dim != 64) return fail(WENC_ERR_UNSUPPORTED, "head_dim %d: only 64 is implemented", c->head_dim);
+  if (c->d_model % 128 != 0 || !wenc_host::layernorm_supported(c->d_model))
+    return fail(WENC_ERR_UNSUPPORTED, "d_model %d: must be a multiple of 128, at most 2048", c->d_model);
+  if (c->ffn_dim % 128 != 0) return fail(WENC_ERR_UNSUPPORTED, "ffn_dim %d: must be a multiple of 128", c->ffn_dim);
+  if (c->seq_len > 4096) return fail(WENC_ERR_UNSUPPORTED, "seq_len %d > 4096", c->seq_len);
+  if (static_cast<long long>(c->max_batch) * c->seq_len > (1LL << 28))
+    return fail(WENC_ERR_UNSUPPORTED, "max_batch * seq_len too large");
+  if (!(c->ln_eps >= 0.0f)) return fail(WENC_ERR_INVALID_ARG, "ln_eps must be >= 0");
+  if (c->weight_dtype != WENC_DTYPE_F32 && c->weight_dtype != WENC_DTYPE_BF16)
+    return fail(WENC_ERR_INVALID_ARG, "weight_dtype %d unknown", c->weight_dtype);
+  if (c->precision != WENC_PREC_BF16) return fail(WENC_ERR_UNSUPPORTED, "precision %d: only BF16", c->precision);
+  return WENC_OK;
+}
+
+void free_handle(wenc* h) {
+  if (!h) return;
+  if (h->weight_arena) cudaFree(h->weight_arena);
+  if (h->work_arena) cudaFree(h->work_arena);
+  if (h->err_host) cudaFreeHost(h->err_host);
+  delete h;
+}
+
+// Copy (bf16 source) or round (f32 source) one matrix into the packed bf16 arena.
+cudaError_t pack_matrix(const void* src, int dtype, uint16_t* dst, size_t n, cudaStream_t s) {
+  if (dtype == WENC_DTYPE_BF16) return cudaMemcpyAsync(dst, src, n * 2, cudaMemcpyDeviceToDevice, s);
+  return wenc_host::launch_f32_to_bf16(static_cast<const float*>(src), dst, n, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* wenc_last_error(void) { return g_last_error.c_str(); }
+
+const char* wenc_version(void) { return "wenc 0.1 sm_103a"; }
+
+wenc_status wenc_create(const wenc_config* cfg, const wenc_layer_weights* layers, const float* lnf_w,
+                        const float* lnf_b, wenc_stream_t stream_, wenc** out) {
+  g_last_error.clear();
+  if (!out) return fail(WENC_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  wenc_status st = check_config(cfg);
+  if (st != WENC_OK) return st;
+  if (!layers) return fail(WENC_ERR_INVALID_ARG, "layers is NULL");
+  std::string why;
+  if (!device_is_sm103(&why)) return fail(WENC_ERR_UNSUPPORTED, "%s", why.c_str());
+  const int L = cfg->n_layers, d = cfg->d_model, f = cfg->ffn_dim;
+  for (int l = 0; l < L; ++l) {
+    const wenc_layer_weights& w = layers[l];
+    const void* req[] = {w.ln1_w, w.ln1_b, w.wq, w.bq, w.wk, w.wv, w.bv, w.wo, w.bo,
+                         w.ln2_w, w.ln2_b, w.w1, w.b1, w.w2, w.b2};
+    for (const void* p : req) {
+      if (!p) return fail(WENC_ERR_INVALID_ARG, "layer %d: a required weight pointer is NULL", l);
+      if (!is_device_accessible(p)) return fail(WENC_ERR_INVALID_ARG, "layer %d: a weight pointer is not device memory", l);
+    }
+    if (w.bk) return fail(WENC_ERR_INVALID_ARG, "layer %d: bk must be NULL (the K projection has no bias)", l);
+  }
+  if (cfg->final_ln && (!lnf_w || !lnf_b)) return fail(WENC_ERR_INVALID_ARG, "final_ln set but lnf_w/lnf_b NULL");
+  if (cfg->final_ln && (!is_device_accessible(lnf_w) || !is_device_accessible(lnf_b)))
+    return fail(WENC_ERR_INVALID_ARG, "lnf_w/lnf_b are not device memory");
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream_);
+  wenc* h = new wenc();
+  h->cfg = *cfg;
+  cudaGetDevice(&h->device);
+  h->num_sms = sm_count();
+  h->bn_qkv = wenc_host::gemm_pick_bn(3 * d);
+  h->bn_o = wenc_host::gemm_pick_bn(d);
+  h->bn_1 = wenc_host::gemm_pick_bn(f);
+  h->bn_2 = wenc_host::gemm_pick_bn(d);
+
+  // ---- weights arena
+  Arena wa;
+  struct Off { size_t wqkv, wo, w1, w2, ln1_w, ln1_b, bqkv, bo, ln2_w, ln2_b, b1, b2; };
+  std::vector<Off> offs(L);
+  for (int l = 0; l < L; ++l) {
+    Off& o = offs[l];
+    o.wqkv = wa.take(size_t(3) * d * d * 2);
+    o.wo = wa.take(size_t(d) * d * 2);
+    o.w1 = wa.take(size_t(f) * d * 2);
+    o.w2 = wa.take(size_t(d) * f * 2);
+    o.ln1_w = wa.take(d * 4); o.ln1_b = wa.take(d * 4);
+    o.bqkv = wa.take(3 * d * 4); o.bo = wa.take(d * 4);
+    o.ln2_w = wa.take(d * 4); o.ln2_b = wa.take(d * 4);
+    o.b1 = wa.take(f * 4); o.b2 = wa.take(d * 4);
+  }
+  const size_t off_lnf_w = wa.take(d * 4), off_lnf_b = wa.take(d * 4);
+  cudaError_t e = cudaMalloc(&h->weight_arena, wa.used);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    free_handle(h);
+    return fail(WENC_ERR_OOM, "weights: cudaMalloc(%zu) failed", wa.used);
+  }
+  uint8_t* wb = static_cast<uint8_t*>(h->weight_arena);
+
+  // ---- workspace arena
+  const size_t rows = size_t(cfg->max_batch) * cfg->seq_len;
+  Arena ka;
+  const size_t off_x = ka.take(rows * d * 4), off_xn = ka.take(rows * d * 2), off_qkv = ka.take(rows * 3 * d * 2),
+               off_o = ka.take(rows * d * 2), off_u = ka.take(rows * f * 2);
+  e = cudaMalloc(&h->work_arena, ka.used);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    free_handle(h);
+    return fail(WENC_ERR_OOM, "workspace: cudaMalloc(%zu) failed", ka.used);
+  }
+  uint8_t* kb = static_cast<uint8_t*>(h->work_arena);
+  h->x = reinterpret_cast<float*>(kb + off_x);
+  h->xn = reinterpret_cast<uint16_t*>(kb + off_xn);
+  h->qkv = reinterpret_cast<uint16_t*>(kb + off_qkv);
+  h->o = reinterpret_cast<uint16_t*>(kb + off_o);
+  h->u = reinterpret_cast<uint16_t*>(kb + off_u);
+
+  e = cudaHostAlloc(reinterpret_cast<void**>(&h->err_host), sizeof(uint32_t), cudaHostAllocMapped);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    free_handle(h);
+    return fail(WENC_ERR_OOM, "error word: cudaHostAlloc failed");
+  }
+  *h->err_host = 0;
+  cudaHostGetDevicePointer(reinterpret_cast<void**>(&h->err_dev), h->err_host, 0);
+
+  // ---- pack weights
+  h->layers.resize(L);
+  for (int l = 0; l < L && e == cudaSuccess; ++l) {
+    const wenc_layer_weights& w = layers[l];
+    const Off& o = offs[l];
+    wenc::Layer& P = h->layers[l];
+    P.wqkv = reinterpret_cast<uint16_t*>(wb + o.wqkv);
+    P.wo = reinterpret_cast<uint16_t*>(wb + o.wo);
+    P.w1 = reinterpret_cast<uint16_t*>(wb + o.w1);
+    P.w2 = reinterpret_cast<uint16_t*>(wb + o.w2);
+    P.ln1_w = reinterpret_cast<float*>(wb + o.ln1_w);
+    P.ln1_b = reinterpret_cast<float*>(wb + o.ln1_b);
+    P.bqkv = reinterpret_cast<float*>(wb + o.bqkv);
+    P.bo = reinterpret_cast<float*>(wb + o.bo);
+    P.ln2_w = reinterpret_cast<float*>(wb + o.ln2_w);
+    P.ln2_b = reinterpret_cast<float*>(wb + o.ln2_b);
+    P.b1 = reinterpret_cast<float*>(wb + o.b1);
+    P.b2 = reinterpret_cast<float*>(wb + o.b2);
+    const size_t dd = size_t(d) * d;
+    if (e == cudaSuccess) e = pack_matrix(w.wq, cfg->weight_dtype, P.wqkv, dd, s);
+    if (e == cudaSuccess) e = pack_matrix(w.wk, cfg->weight_dtype, P.wqkv + dd, dd, s);
+    if (e == cudaSuccess) e = pack_matrix(w.wv, cfg->weight_dtype, P.wqkv + 2 * dd, dd, s);
+    if (e == cudaSuccess) e = pack_matrix(w.wo, cfg->weight_dtype, P.wo, dd, s);
+    if (e == cudaSuccess) e = pack_matrix(w.w1, cfg->weight_dtype, P.w1, size_t(f) * d, s);
+    if (e == cudaSuccess) e = pack_matrix(w.w2, cfg->weight_dtype, P.w2, size_t(d) * f, s);
+    auto cp = [&](float* dst, const float* src, size_t n) {
+      if (e == cudaSuccess) e = cudaMemcpyAsync(dst, src, n * 4, cudaMemcpyDeviceToDevice, s);
+    };
+    cp(P.ln1_w, w.ln1_w, d); cp(P.ln1_b, w.ln1_b, d);
+    cp(P.bqkv, w.bq, d);
+    if (e == cudaSuccess) e = cudaMemsetAsync(P.bqkv + d, 0, size_t(d) * 4, s);  // K has no bias
+    cp(P.bqkv + 2 * d, w.bv, d);
+    cp(P.bo, w.bo, d);
+    cp(P.ln2_w, w.ln2_w, d); cp(P.ln2_b, w.ln2_b, d);
+    cp(P.b1, w.b1, f); cp(P.b2, w.b2, d);
+  }
+  if (cfg->final_ln && e == cudaSuccess) {
+    h->lnf_w = reinterpret_cast<float*>(wb + off_lnf_w);
+    h->lnf_b = reinterpret_cast<float*>(wb + off_lnf_b);
+    e = cudaMemcpyAsync(h->lnf_w, lnf_w, d * 4, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(h->lnf_b, lnf_b, d * 4, cudaMemcpyDeviceToDevice, s);
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) {
+    free_handle(h);
+    return cuda_fail(e, "packing weights");
+  }
+
+  // ---- tensor maps (all over library-owned buffers; built once)
+  bool ok = true;
+  for (int l = 0; l < L && ok; ++l) {
+    wenc::Layer& P = h->layers[l];
+    ok = ok && wenc_host::make_tmap_2d_bf16(&P.tm_wqkv, P.wqkv, d, 3 * d, size_t(d) * 2, 64, h->bn_qkv, &why);
+    ok = ok && wenc_host::make_tmap_2d_bf16(&P.tm_wo, P.wo, d, d, size_t(d) * 2, 64, h->bn_o, &why);
+    ok = ok && wenc_host::make_tmap_2d_bf16(&P.tm_w1, P.w1, d, f, size_t(d) * 2, 64, h->bn_1, &why);
+    ok = ok && wenc_host::make_tmap_2d_bf16(&P.tm_w2, P.w2, f, d, size_t(f) * 2, 64, h->bn_2, &why);
+  }
+  ok = ok && wenc_host::make_tmap_2d_bf16(&h->tm_xn, h->xn, d, rows, size_t(d) * 2, 64, wenc_host::kGemmBM, &why);
+  ok = ok && wenc_host::make_tmap_2d_bf16(&h->tm_o, h->o, d, rows, size_t(d) * 2, 64, wenc_host::kGemmBM, &why);
+  ok = ok && wenc_host::make_tmap_2d_bf16(&h->tm_u, h->u, f, rows, size_t(f) * 2, 64, wenc_host::kGemmBM, &why);
+  const size_t qkv_row = size_t(3) * d * 2;
+  ok = ok && wenc_host::make_tmap_3d_bf16(&h->tm_q, h->qkv, 3 * d, cfg->seq_len, cfg->max_batch, qkv_row,
+                                          qkv_row * cfg->seq_len, 64, wenc_host::kAttnBQ, &why);
+  ok = ok && wenc_host::make_tmap_3d_bf16(&h->tm_kv, h->qkv, 3 * d, cfg->seq_len, cfg->max_batch, qkv_row,
+                                          qkv_row * cfg->seq_len, 64, wenc_host::kAttnBKV, &why);
+  if (!ok) {
+    free_handle(h);
+    return fail(WENC_ERR_CUDA, "%s", why.c_str());
+  }
+  *out = h;
+  return WENC_OK;
+}
+
+int wenc_forward_launches(const wenc* h, int first, int count, int apply_final_ln) {
+  if (!h || first < 0 || count < 0 || first + count > h->cfg.n_layers) return -1;
+  const bool final_ln = apply_final_ln && h->cfg.final_ln;
+  int n = 7 * count;
+  if (final_ln) n += 1;
+  else if (count == 0) n += 1;  // the copy in -> out
+  return n;
+}
+
+wenc_status wenc_set_launch_events(wenc* h, void* const* events, int n_events, int* kinds) {
+  if (!h) return fail(WENC_ERR_INVALID_ARG, "handle is NULL");
+  h->events.clear();
+  h->kinds = kinds;
+  if (events) {
+    if (n_events < 1) return fail(WENC_ERR_INVALID_ARG, "n_events < 1");
+    for (int i = 0; i < n_events; ++i) h->events.push_back(static_cast<cudaEvent_t>(events[i]));
+  }
+  return WENC_OK;
+}
+
+wenc_status wenc_forward_layers(wenc* h, const float* in, float* out, int B, int first, int count, int apply_final_ln,
+                                wenc_stream_t stream_) {
+  g_last_error.clear();
+  if (!h) return fail(WENC_ERR_INVALID_ARG, "handle is NULL");
+  const wenc_config& c = h->cfg;
+  if (!in || !out) return fail(WENC_ERR_INVALID_ARG, "hidden_in/hidden_out is NULL");
+  if (!aligned16(in) || !aligned16(out)) return fail(WENC_ERR_INVALID_ARG, "hidden buffers must be 16-byte aligned");
+  if (B < 1 || B > c.max_batch) return fail(WENC_ERR_INVALID_ARG, "B = %d outside 1..max_batch %d", B, c.max_batch);
+  if (first < 0 || count < 0 || first + count > c.n_layers)
+    return fail(WENC_ERR_INVALID_ARG, "layers %d..%d outside 0..%d", first, first + count - 1, c.n_layers - 1);
+  int dev = -1;
+  cudaGetDevice(&dev);
+  if (dev != h->device) return fail(WENC_ERR_INVALID_ARG, "current device %d is not the handle's device %d", dev, h->device);
+  if (*reinterpret_cast<volatile uint32_t*>(h->err_host) != 0)
+    return fail(WENC_ERR_DEVICE_TIMEOUT, "an earlier launch recorded device error word 0x%x",
+                *reinterpret_cast<volatile uint32_t*>(h->err_host));
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream_);
+  const int d = c.d_model, f = c.ffn_dim, T = c.seq_len, H = c.n_heads;
+  const int M = B * T;
+  const bool final_ln = apply_final_ln && c.final_ln;
+  const int n_launch = wenc_forward_launches(h, first, count, apply_final_ln);
+  std::vector<cudaEvent_t> ev;
+  ev.swap(h->events);
+  int* kinds = h->kinds;
+  h->kinds = nullptr;
+  if (!ev.empty() && static_cast<int>(ev.size()) < n_launch + 1)
+    return fail(WENC_ERR_INVALID_ARG, "launch events: need %d, got %zu", n_launch + 1, ev.size());
+
+  int li = 0;
+  cudaError_t e = cudaSuccess;
+  auto rec = [&](int kind, cudaError_t le) {
+    if (e == cudaSuccess) e = le;
+    if (kinds) kinds[li] = kind;
+    ++li;
+    if (!ev.empty() && e == cudaSuccess) e = cudaEventRecord(ev[li], s);
+  };
+  if (!ev.empty()) e = cudaEventRecord(ev[0], s);
+
+  const float* src = in;  // the residual stream entering the next block
+  for (int l = first; l < first + count && e == cudaSuccess; ++l) {
+    const wenc::Layer& P = h->layers[l];
+    const bool last = (l == first + count - 1);
+    float* dst_final = (last && !final_ln) ? out : h->x;
+    rec(0, wenc_host::launch_layernorm(src, P.ln1_w, P.ln1_b, h->xn, M, d, c.ln_eps, true, s));
+    rec(1, wenc_host::launch_gemm(h->tm_xn, P.tm_wqkv, M, 3 * d, d, h->bn_qkv, WENC_EPI_BIAS_BF16, P.bqkv, nullptr,
+                                  h->qkv, h->err_dev, h->num_sms, s));
+    rec(2, wenc_host::launch_attention(h->tm_q, h->tm_kv, h->tm_kv, 0, d, 2 * d, h->o, d, B, T, H, h->err_dev, s));
+    rec(3, wenc_host::launch_gemm(h->tm_o, P.tm_wo, M, d, d, h->bn_o, WENC_EPI_BIAS_RESID_F32, P.bo, src, h->x,
+                                  h->err_dev, h->num_sms, s));
+    rec(0, wenc_host::launch_layernorm(h->x, P.ln2_w, P.ln2_b, h->xn, M, d, c.ln_eps, true, s));
+    rec(4, wenc_host::launch_gemm(h->tm_xn, P.tm_w1, M, f, d, h->bn_1, WENC_EPI_BIAS_GELU_BF16, P.b1, nullptr, h->u,
+                                  h->err_dev, h->num_sms, s));
+    rec(5, wenc_host::launch_gemm(h->tm_u, P.tm_w2, M, d, f, h->bn_2, WENC_EPI_BIAS_RESID_F32, P.b2, h->x, dst_final,
+                                  h->err_dev, h->num_sms, s));
+    src = h->x;
+  }
+  if (e == cudaSuccess) {
+    if (final_ln) {
+      rec(6, wenc_host::launch_layernorm(src, h->lnf_w, h->lnf_b, out, M, d, c.ln_eps, false, s));
+    } else if (count == 0) {
+      rec(7, in == out ? cudaSuccess : cudaMemcpyAsync(out, in, size_t(M) * d * 4, cudaMemcpyDeviceToDevice, s));
+    }
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+  return WENC_OK;
+}
+
+wenc_status wenc_forward(wenc* h, const float* in, float* out, int B, wenc_stream_t stream) {
+  if (!h) return fail(WENC_ERR_INVALID_ARG, "handle is NULL");
+  return wenc_forward_layers(h, in, out, B, 0, h->cfg.n_layers, 1, stream);
+}
+
+wenc_status wenc_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* out, int B, int T, int H,
+                           int hd, wenc_stream_t stream) {
+  g_last_error.clear();
+  if (!q || !k || !v || !out) return fail(WENC_ERR_INVALID_ARG, "q/k/v/out is NULL");
+  if (B < 1 || T < 1 || H < 1) return fail(WENC_ERR_INVALID_ARG, "B, T, H must be >= 1");
+  if (hd != 64) return fail(WENC_ERR_UNSUPPORTED, "head_dim %d: only 64 is implemented", hd);
+  if (T > (1 << 20)) return fail(WENC_ERR_UNSUPPORTED, "T %d too large", T);
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(WENC_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
+  std::string why;
+  if (!device_is_sm103(&why)) return fail(WENC_ERR_UNSUPPORTED, "%s", why.c_str());
+  uint32_t* err = global_error_word(&why);
+  if (!err) return fail(WENC_ERR_CUDA, "%s", why.c_str());
+  const uint64_t row = uint64_t(H) * 64;
+  CUtensorMap tq, tk, tv;
+  bool ok = wenc_host::make_tmap_3d_bf16(&tq, q, row, T, B, row * 2, row * 2 * T, 64, wenc_host::kAttnBQ, &why) &&
+            wenc_host::make_tmap_3d_bf16(&tk, k, row, T, B, row * 2, row * 2 * T, 64, wenc_host::kAttnBKV, &why) &&
+            wenc_host::make_tmap_3d_bf16(&tv, v, row, T, B, row * 2, row * 2 * T, 64, wenc_host::kAttnBKV, &why);
+  if (!ok) return fail(WENC_ERR_INVALID_ARG, "%s", why.c_str());
+  cudaError_t e = wenc_host::launch_attention(tq, tk, tv, 0, 0, 0, out, static_cast<int>(row), B, T, H, err,
+                                              reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+  return WENC_OK;
+}
+
+wenc_status wenc_layernorm(const float* x, const float* w, const float* b, void* y, int rows, int d, float eps,
+                           int out_bf16, wenc_stream_t stream) {
+  g_last_error.clear();
+  if (!x || !w || !b || !y) return fail(WENC_ERR_INVALID_ARG, "x/w/b/y is NULL");
+  if (rows < 1) return fail(WENC_ERR_INVALID_ARG, "rows must be >= 1");
+  if (!wenc_host::layernorm_supported(d)) return fail(WENC_ERR_UNSUPPORTED, "d %d: a multiple of 128 up to 2048", d);
+  if (!(eps >= 0.0f)) return fail(WENC_ERR_INVALID_ARG, "eps must be >= 0");
+  if (!aligned16(x) || !aligned16(w) || !aligned16(b) || !aligned16(y))
+    return fail(WENC_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
+  cudaError_t e = wenc_host::launch_layernorm(x, w, b, y, rows, d, eps, out_bf16 != 0, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "layernorm launch");
+  return WENC_OK;
+}
+
+wenc_status wenc_linear(const uint16_t* A, const uint16_t* W, const float* bias, const float* resid, void* out, int M,
+                        int N, int K, int epilogue, wenc_stream_t stream) {
+  g_last_error.clear();
+  if (!A || !W || !bias || !out) return fail(WENC_ERR_INVALID_ARG, "A/W/bias/out is NULL");
+  if (epilogue < 0 || epilogue > 2) return fail(WENC_ERR_INVALID_ARG, "epilogue %d unknown", epilogue);
+  if (epilogue == WENC_EPI_BIAS_RESID_F32 && !resid) return fail(WENC_ERR_INVALID_ARG, "resid is NULL");
+  if (M < 1) return fail(WENC_ERR_INVALID_ARG, "M must be >= 1");
+  const int bn = wenc_host::gemm_pick_bn(N);
+  if (bn == 0) return fail(WENC_ERR_UNSUPPORTED, "N %d: must be a multiple of 128", N);
+  if (K < 64 || K % 64 != 0) return fail(WENC_ERR_UNSUPPORTED, "K %d: must be a positive multiple of 64", K);
+  if (!aligned16(A) || !aligned16(W) || !aligned16(bias) || !aligned16(out) || (resid && !aligned16(resid)))
+    return fail(WENC_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
+  std::string why;
+  if (!device_is_sm103(&why)) return fail(WENC_ERR_UNSUPPORTED, "%s", why.c_str());
+  uint32_t* err = global_error_word(&why);
+  if (!err) return fail(WENC_ERR_CUDA, "%s", why.c_str());
+  CUtensorMap ta, tw;
+  bool ok = wenc_host::make_tmap_2d_bf16(&ta, A, K, M, size_t(K) * 2, 64, wenc_host::kGemmBM, &why) &&
+            wenc_host::make_tmap_2d_bf16(&tw, W, K, N, size_t(K) * 2, 64, bn, &why);
+  if (!ok) return fail(WENC_ERR_INVALID_ARG, "%s", why.c_str());
+  cudaError_t e = wenc_host::launch_gemm(ta, tw, M, N, K, bn, epilogue, bias, resid, out, err, sm_count(),
+                                         reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "linear launch");
+  return WENC_OK;
+}
+
+wenc_status wenc_sync_status(wenc* h) {
+  g_last_error.clear();
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  uint32_t word = 0;
+  if (h) {
+    word = *reinterpret_cast<volatile uint32_t*>(h->err_host);
+    *reinterpret_cast<volatile uint32_t*>(h->err_host) = 0;
+  } else {
+    std::string why;
+    if (!global_error_word(&why)) return fail(WENC_ERR_CUDA, "%s", why.c_str());
+    e = cudaMemcpyFromSymbol(&word, g_device_error_word, sizeof(word));
+    if (e == cudaSuccess && word != 0) {
+      const uint32_t zero = 0;
+      e = cudaMemcpyToSymbol(g_device_error_word, &zero, sizeof(zero));
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  }
+  if (word != 0)
+    return fail(WENC_ERR_DEVICE_TIMEOUT, "device wait ran out (code %u, site %u)", word & 0xffu, (word >> 8) & 0xffu);
+  return WENC_OK;
+}
+
+void wenc_destroy(wenc* h) {
+  if (!h) return;
+  cudaDeviceSynchronize();
+  free_handle(h);
+}
+
+}  // extern "C"

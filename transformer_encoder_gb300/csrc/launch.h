@@ -1,0 +1,51 @@
+// launch.h -- host-side launchers of the kernels (internal to libwenc.so).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+
+namespace wenc_host {
+
+// Tensor-map construction (cuTensorMapEncodeTiled through the runtime's driver entry
+// point, so the library does not link libcuda directly).
+// 2-D bf16 view: `outer` rows of `inner` elements, rows `row_stride_bytes` apart; the box is
+// box_inner x box_outer elements, 128-byte swizzled (box_inner * 2 must be 128).
+bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                       uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, std::string* why);
+// 3-D bf16 view [dim2][dim1][inner] with explicit strides (bytes) for dims 1 and 2.
+bool make_tmap_3d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t dim1, uint64_t dim2,
+                       uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box_inner, uint32_t box1,
+                       std::string* why);
+
+// ---------------------------------------------------------------- LayerNorm
+bool layernorm_supported(int d);
+cudaError_t launch_layernorm(const float* x, const float* w, const float* b, void* y, int rows, int d, float eps,
+                             bool out_bf16, cudaStream_t stream);
+
+// ---------------------------------------------------------------- GEMM (tcgen05)
+// C[M, N] = A[M, K] * W[N, K]^T with a fused epilogue (wenc_epilogue values).
+// Tile: 128 x bn (bn = 256 or 128), k-block 64. tmA: box 64 x 128 over A; tmW: box 64 x bn over W.
+int gemm_pick_bn(int N);  // 0 if N is unsupported
+constexpr int kGemmBM = 128;
+constexpr int kGemmBK = 64;
+cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmW, int M, int N, int K, int bn, int epilogue,
+                        const float* bias, const float* resid, void* out, uint32_t* err, int num_sms,
+                        cudaStream_t stream);
+
+// ---------------------------------------------------------------- attention (tcgen05)
+// Q/K/V tiles are read through 3-D maps [B][T][row] (box 64 x 128 for Q, 64 x 64 for K, V);
+// head h of Q, K, V starts at column q_col0 + 64h, k_col0 + 64h, v_col0 + 64h.
+// out: bf16, row (b*T + t) at out + (b*T+t)*out_stride + 64h.
+constexpr int kAttnBQ = 128;
+constexpr int kAttnBKV = 64;
+cudaError_t launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, int q_col0,
+                             int k_col0, int v_col0, uint16_t* out, int out_stride, int B, int T, int H,
+                             uint32_t* err, cudaStream_t stream);
+
+// ---------------------------------------------------------------- weight packing
+cudaError_t launch_f32_to_bf16(const float* src, uint16_t* dst, size_t n, cudaStream_t stream);
+
+}  // namespace wenc_host

@@ -1,0 +1,118 @@
+// ln.cu -- LayerNorm over rows of the fp32 residual stream, and the weight-packing cast.
+//
+// y = (x - mean) / sqrt(var + eps) * w + b with the biased variance (inferencelayer 0.2.4
+// src/whisper_gpu.rs, LN_SRC; turbospark-runtime 0.3.0 src/whisper/metal.rs, the
+// encode_whisper_layer_norm calls of encode_layer and encode_partial; oxinfer 0.0.5
+// src/whisper/model.rs, LayerNorm::apply_rows with LN_EPS).
+//
+// One warp per row: the row is read once from HBM with coalesced 16-byte loads and kept in
+// registers, the mean and then the sum of squared deviations are reduced with shuffles (two
+// passes over registers, one pass over memory), and the output is written as bf16 (feeding
+// the next GEMM's TMA loads: LayerNorm and the operand cast fused) or fp32 (the final LN).
+#include <cuda_bf16.h>
+
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace {
+
+constexpr int kRowsPerBlock = 8;  // 8 warps, one row each
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// NV = d / 128: float4 loads per lane.
+template <int NV, bool OUT_BF16>
+__global__ void __launch_bounds__(32 * kRowsPerBlock)
+    layernorm_kernel(const float* __restrict__ x, const float* __restrict__ w, const float* __restrict__ b,
+                     void* __restrict__ y, int rows, float eps) {
+  constexpr int D = NV * 128;
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const float4* xr = reinterpret_cast<const float4*>(x + static_cast<size_t>(row) * D);
+  float4 v[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) v[i] = xr[lane + 32 * i];
+  float s = 0.0f;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+  const float mean = warp_sum(s) * (1.0f / D);
+  float q = 0.0f;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const float a = v[i].x - mean, bb = v[i].y - mean, c = v[i].z - mean, d = v[i].w - mean;
+    q += (a * a + bb * bb) + (c * c + d * d);
+  }
+  const float var = warp_sum(q) * (1.0f / D);
+  const float rstd = 1.0f / sqrtf(var + eps);
+  const float4* w4 = reinterpret_cast<const float4*>(w);
+  const float4* b4 = reinterpret_cast<const float4*>(b);
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int c4 = lane + 32 * i;
+    const float4 ww = __ldg(w4 + c4), bb = __ldg(b4 + c4);
+    float4 o;
+    o.x = (v[i].x - mean) * rstd * ww.x + bb.x;
+    o.y = (v[i].y - mean) * rstd * ww.y + bb.y;
+    o.z = (v[i].z - mean) * rstd * ww.z + bb.z;
+    o.w = (v[i].w - mean) * rstd * ww.w + bb.w;
+    if constexpr (OUT_BF16) {
+      uint2 pk = make_uint2(wenc_dev::pack_bf16x2(o.x, o.y), wenc_dev::pack_bf16x2(o.z, o.w));
+      reinterpret_cast<uint2*>(static_cast<uint16_t*>(y) + static_cast<size_t>(row) * D)[c4] = pk;
+    } else {
+      reinterpret_cast<float4*>(static_cast<float*>(y) + static_cast<size_t>(row) * D)[c4] = o;
+    }
+  }
+}
+
+template <int NV>
+cudaError_t launch_nv(const float* x, const float* w, const float* b, void* y, int rows, float eps, bool out_bf16,
+                      cudaStream_t stream) {
+  const int grid = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
+  if (out_bf16)
+    layernorm_kernel<NV, true><<<grid, 32 * kRowsPerBlock, 0, stream>>>(x, w, b, y, rows, eps);
+  else
+    layernorm_kernel<NV, false><<<grid, 32 * kRowsPerBlock, 0, stream>>>(x, w, b, y, rows, eps);
+  return cudaGetLastError();
+}
+
+__global__ void f32_to_bf16_kernel(const float* __restrict__ src, uint16_t* __restrict__ dst, size_t n) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    __nv_bfloat16 v = __float2bfloat16_rn(src[i]);  // round to nearest, ties to even
+    dst[i] = *reinterpret_cast<uint16_t*>(&v);
+  }
+}
+
+}  // namespace
+
+namespace wenc_host {
+
+bool layernorm_supported(int d) { return d > 0 && d % 128 == 0 && d / 128 <= 16; }
+
+cudaError_t launch_layernorm(const float* x, const float* w, const float* b, void* y, int rows, int d, float eps,
+                             bool out_bf16, cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  switch (d / 128) {
+#define WENC_LN_CASE(N) \
+  case N: return launch_nv<N>(x, w, b, y, rows, eps, out_bf16, stream);
+    WENC_LN_CASE(1) WENC_LN_CASE(2) WENC_LN_CASE(3) WENC_LN_CASE(4) WENC_LN_CASE(5) WENC_LN_CASE(6)
+    WENC_LN_CASE(7) WENC_LN_CASE(8) WENC_LN_CASE(9) WENC_LN_CASE(10) WENC_LN_CASE(11) WENC_LN_CASE(12)
+    WENC_LN_CASE(13) WENC_LN_CASE(14) WENC_LN_CASE(15) WENC_LN_CASE(16)
+#undef WENC_LN_CASE
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_f32_to_bf16(const float* src, uint16_t* dst, size_t n, cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  const size_t blocks = (n + 255) / 256;
+  f32_to_bf16_kernel<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(src, dst, n);
+  return cudaGetLastError();
+}
+
+}  // namespace wenc_host

@@ -1,0 +1,238 @@
+"""Thin ctypes binding of libwenc.so (argument marshalling only).
+
+Every step of the encoder runs in the library's CUDA kernels; this module only turns
+PyTorch tensors (used here for device memory and streams) into the pointers and sizes
+of the C ABI declared in include/wenc.h, and turns non-OK statuses into exceptions.
+There is no fallback: if the library is missing or the device is not sm_103a, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "WencError", "lib", "lib_path", "Encoder", "attention", "layernorm", "linear", "sync_status",
+    "EPI_BIAS_BF16", "EPI_BIAS_GELU_BF16", "EPI_BIAS_RESID_F32", "EXPORTED_SYMBOLS",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+lib_path = os.path.join(_PKG, "_lib", "libwenc.so")
+
+EPI_BIAS_BF16, EPI_BIAS_GELU_BF16, EPI_BIAS_RESID_F32 = 0, 1, 2
+_STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "OOM", 4: "CUDA", 5: "DEVICE_TIMEOUT"}
+LAUNCH_KINDS = {0: "layernorm", 1: "gemm_qkv", 2: "attention", 3: "gemm_out", 4: "gemm_fc1", 5: "gemm_fc2",
+                6: "layernorm_final", 7: "copy"}
+
+EXPORTED_SYMBOLS = (
+    "wenc_create", "wenc_forward", "wenc_forward_layers", "wenc_forward_launches", "wenc_set_launch_events",
+    "wenc_attention", "wenc_layernorm", "wenc_linear", "wenc_sync_status", "wenc_destroy", "wenc_last_error",
+    "wenc_version",
+)
+
+
+class WencError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"wenc {_STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int), ("d_model", ctypes.c_int), ("n_heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("ffn_dim", ctypes.c_int), ("seq_len", ctypes.c_int),
+                ("max_batch", ctypes.c_int), ("final_ln", ctypes.c_int), ("ln_eps", ctypes.c_float),
+                ("weight_dtype", ctypes.c_int), ("precision", ctypes.c_int)]
+
+
+_LW_FIELDS = ("ln1_w", "ln1_b", "wq", "bq", "wk", "bk", "wv", "bv", "wo", "bo", "ln2_w", "ln2_b", "w1", "b1", "w2", "b2")
+
+
+class LayerWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in _LW_FIELDS]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libwenc.so (built in-tree by transformer_encoder_gb300.build); raise if absent."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(lib_path):
+            raise RuntimeError(f"{lib_path} is missing: build it with `python -m transformer_encoder_gb300.build`")
+        L = ctypes.CDLL(lib_path)
+        vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        L.wenc_create.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(LayerWeights), vp, vp, vp, ctypes.POINTER(vp)]
+        L.wenc_forward.argtypes = [vp, vp, vp, i, vp]
+        L.wenc_forward_layers.argtypes = [vp, vp, vp, i, i, i, i, vp]
+        L.wenc_forward_launches.argtypes = [vp, i, i, i]
+        L.wenc_set_launch_events.argtypes = [vp, ctypes.POINTER(vp), i, ctypes.POINTER(i)]
+        L.wenc_attention.argtypes = [vp, vp, vp, vp, i, i, i, i, vp]
+        L.wenc_layernorm.argtypes = [vp, vp, vp, vp, i, i, f, i, vp]
+        L.wenc_linear.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, vp]
+        L.wenc_sync_status.argtypes = [vp]
+        L.wenc_destroy.argtypes = [vp]
+        L.wenc_destroy.restype = None
+        L.wenc_last_error.restype = ctypes.c_char_p
+        L.wenc_version.restype = ctypes.c_char_p
+        for name in ("wenc_create", "wenc_forward", "wenc_forward_layers", "wenc_set_launch_events", "wenc_attention",
+                     "wenc_layernorm", "wenc_linear", "wenc_sync_status", "wenc_forward_launches"):
+            getattr(L, name).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _check(status: int):
+    if status != 0:
+        raise WencError(status, lib().wenc_last_error().decode(errors="replace"))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _require(t, dtype, name):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+class Encoder:
+    """A wenc handle: packed resident weights plus a workspace for `max_batch` windows.
+
+    ``layers`` is a list of dicts with the keys of ``synth.LAYER_KEYS`` holding CUDA tensors
+    (matrices float32 or bfloat16 [n_out, n_in], vectors float32). The library copies and
+    packs them, so they may be freed after construction.
+    """
+
+    def __init__(self, layers, n_heads: int, seq_len: int, max_batch: int, final=None, ln_eps: float = 1e-5,
+                 stream=None):
+        import torch
+        L = lib()
+        d = layers[0]["wq"].shape[0]
+        f = layers[0]["w1"].shape[0]
+        mdtype = layers[0]["wq"].dtype
+        if mdtype not in (torch.float32, torch.bfloat16):
+            raise TypeError("weight matrices must be float32 or bfloat16")
+        cfg = Config(len(layers), d, n_heads, d // n_heads, f, seq_len, max_batch, 1 if final is not None else 0,
+                     ln_eps, 1 if mdtype == torch.bfloat16 else 0, 0)
+        arr = (LayerWeights * len(layers))()
+        for i, p in enumerate(layers):
+            for k in ("wq", "wk", "wv", "wo", "w1", "w2"):
+                _require(p[k], mdtype, k)
+            for k in ("ln1_w", "ln1_b", "bq", "bv", "bo", "ln2_w", "ln2_b", "b1", "b2"):
+                _require(p[k], torch.float32, k)
+            for k in _LW_FIELDS:
+                setattr(arr[i], k, None if k == "bk" else p[k].data_ptr())
+        lnf_w = lnf_b = None
+        if final is not None:
+            _require(final[0], torch.float32, "lnf_w")
+            _require(final[1], torch.float32, "lnf_b")
+            lnf_w, lnf_b = _ptr(final[0]), _ptr(final[1])
+        h = ctypes.c_void_p()
+        _check(L.wenc_create(ctypes.byref(cfg), arr, lnf_w, lnf_b, _stream(stream), ctypes.byref(h)))
+        self._h = h
+        self.cfg = cfg
+        self.d_model, self.ffn_dim, self.n_layers, self.seq_len, self.max_batch = d, f, len(layers), seq_len, max_batch
+
+    @property
+    def handle(self):
+        return self._h
+
+    def forward(self, x, out=None, stream=None):
+        """out = Encoder(x), x float32 CUDA [B, seq_len, d]; out may be x (in place)."""
+        return self.forward_layers(x, out, 0, self.n_layers, True, stream)
+
+    def forward_layers(self, x, out=None, first: int = 0, count: int | None = None, final_ln: bool = True,
+                       stream=None):
+        import torch
+        _require(x, torch.float32, "x")
+        if count is None:
+            count = self.n_layers - first
+        if out is None:
+            out = torch.empty_like(x)
+        _require(out, torch.float32, "out")
+        B = x.shape[0]
+        _check(lib().wenc_forward_layers(self._h, _ptr(x), _ptr(out), B, first, count, int(final_ln), _stream(stream)))
+        return out
+
+    def launches(self, first: int = 0, count: int | None = None, final_ln: bool = True) -> int:
+        count = self.n_layers - first if count is None else count
+        return lib().wenc_forward_launches(self._h, first, count, int(final_ln))
+
+    def set_launch_events(self, events, want_kinds: bool = True):
+        """Arm the per-launch timing hook for the next forward call (torch.cuda.Event list)."""
+        n = len(events)
+        ev = (ctypes.c_void_p * n)(*[e.cuda_event for e in events])
+        kinds = (ctypes.c_int * n)() if want_kinds else None
+        self._ev_keep = (ev, kinds)
+        _check(lib().wenc_set_launch_events(self._h, ev, n, kinds))
+        return kinds
+
+    def sync_status(self):
+        _check(lib().wenc_sync_status(self._h))
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            lib().wenc_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def attention(q, k, v, out=None, stream=None):
+    """out = softmax(q k^T / 8) v per (window, head); q, k, v bf16 CUDA [B, T, H, 64]."""
+    import torch
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _require(t, torch.bfloat16, n)
+    B, T, H, hd = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _require(out, torch.bfloat16, "out")
+    _check(lib().wenc_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, T, H, hd, _stream(stream)))
+    return out
+
+
+def layernorm(x, w, b, eps: float = 1e-5, out_bf16: bool = True, out=None, stream=None):
+    """LayerNorm over the last axis of a float32 CUDA tensor; bf16 or float32 output."""
+    import torch
+    _require(x, torch.float32, "x")
+    d = x.shape[-1]
+    rows = x.numel() // d
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.bfloat16 if out_bf16 else torch.float32, device=x.device)
+    _check(lib().wenc_layernorm(_ptr(x), _ptr(w), _ptr(b), _ptr(out), rows, d, eps, int(out_bf16), _stream(stream)))
+    return out
+
+
+def linear(a, w, bias, epilogue: int = EPI_BIAS_BF16, resid=None, out=None, stream=None):
+    """out = epilogue(a w^T + bias); a bf16 [M, K], w bf16 [N, K], bias float32 [N]."""
+    import torch
+    _require(a, torch.bfloat16, "a")
+    _require(w, torch.bfloat16, "w")
+    _require(bias, torch.float32, "bias")
+    M, K = a.shape
+    N = w.shape[0]
+    if out is None:
+        dt = torch.float32 if epilogue == EPI_BIAS_RESID_F32 else torch.bfloat16
+        out = torch.empty((M, N), dtype=dt, device=a.device)
+    _check(lib().wenc_linear(_ptr(a), _ptr(w), _ptr(bias), _ptr(resid), _ptr(out), M, N, K, epilogue, _stream(stream)))
+    return out
+
+
+def sync_status(encoder: Encoder | None = None):
+    _check(lib().wenc_sync_status(encoder.handle if encoder is not None else None))
