@@ -72,6 +72,9 @@ WORKLOADS = {
     "base_stack": Workload("base_stack", 4, 512, 8, 2048, 6, final_ln=True, bf16_weights=True),
     "small_stack": Workload("small_stack", 8, 768, 12, 3072, 12, final_ln=True, bf16_weights=True),
     "large_stack": Workload("large_stack", 16, 1280, 20, 5120, 32, final_ln=True, bf16_weights=True),
+    # One block at large-v3 dims and batch 16: every kernel launch has exactly the shape it has
+    # inside the 32-block stack, with ~1 GB on the device (used for profiler captures).
+    "large_block": Workload("large_block", 16, 1280, 20, 5120, 1, final_ln=True, bf16_weights=True),
 }
 
 

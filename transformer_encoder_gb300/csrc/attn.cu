@@ -177,18 +177,47 @@ __global__ void __launch_bounds__(kThreads, 2)
       __syncwarp();
       if (lane == 0) mbar_arrive(s_free);
 
-      const int valid = T - j * BKV;  // keys of this tile inside the window
-      float mx = -CUDART_INF_F;
+      float sv[64];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        float s = __uint_as_float(sr[c >> 5][c & 31]);
-        if (c >= valid) s = -CUDART_INF_F;
-        sr[c >> 5][c & 31] = __float_as_uint(s);
-        mx = fmaxf(mx, s);
+      for (int c = 0; c < 64; ++c) sv[c] = __uint_as_float(sr[c >> 5][c & 31]);
+      const int valid = T - j * BKV;  // keys of this tile inside the window
+      if (valid < BKV) {              // only a window's last tile can be partial (warp-uniform)
+#pragma unroll
+        for (int c = 0; c < 64; ++c) sv[c] = (c < valid) ? sv[c] : -CUDART_INF_F;
       }
+      // Row maximum: four independent chains of three-input max.
+      float mc[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        float a = fmax3(sv[16 * k], sv[16 * k + 1], sv[16 * k + 2]);
+#pragma unroll
+        for (int e = 3; e < 15; e += 2) a = fmax3(a, sv[16 * k + e], sv[16 * k + e + 1]);
+        mc[k] = fmaxf(a, sv[16 * k + 15]);
+      }
+      const float mx = fmaxf(fmax3(mc[0], mc[1], mc[2]), mc[3]);
       const float mx_s = mx * scale_log2;
       const float m_new = (mx_s > m + kRescaleThreshold) ? mx_s : m;
       const float alpha = ex2_approx(m - m_new);  // 0 on the first tile (m = -inf)
+
+      // p = 2^(s * scale_log2 - m_new): packed fp32x2 FMA for the argument, packed adds for
+      // the row sum; P is packed to bf16 pairs before waiting on the previous PV product.
+      const uint64_t c2 = pack_f32x2(scale_log2, scale_log2);
+      const uint64_t nm2 = pack_f32x2(-m_new, -m_new);
+      uint64_t sum2a = pack_f32x2(0.0f, 0.0f), sum2b = sum2a;
+      uint32_t pk[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        float a0, a1;
+        unpack_f32x2(fma_f32x2(pack_f32x2(sv[2 * i], sv[2 * i + 1]), c2, nm2), a0, a1);
+        const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+        if (i & 1) sum2b = add_f32x2(sum2b, pack_f32x2(p0, p1));
+        else sum2a = add_f32x2(sum2a, pack_f32x2(p0, p1));
+        pk[i] = pack_bf16x2(p0, p1);
+      }
+      float sa0, sa1, sb0, sb1;
+      unpack_f32x2(sum2a, sa0, sa1);
+      unpack_f32x2(sum2b, sb0, sb1);
+      const float sum = (sa0 + sa1) + (sb0 + sb1);
 
       if (j > 0) {
         // PV of the previous tile must be complete: O is read below and P is overwritten.
@@ -208,21 +237,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       }
 
-      float sum = 0.0f;
       const uint32_t prow = sP + row * 128;
 #pragma unroll
       for (int c8 = 0; c8 < 8; ++c8) {
-        float p[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int c = c8 * 8 + e;
-          p[e] = ex2_approx(fmaf(__uint_as_float(sr[c >> 5][c & 31]), scale_log2, -m_new));
-          sum += p[e];
-        }
-        const uint32_t w0 = pack_bf16x2(p[0], p[1]), w1 = pack_bf16x2(p[2], p[3]);
-        const uint32_t w2 = pack_bf16x2(p[4], p[5]), w3 = pack_bf16x2(p[6], p[7]);
         const uint32_t addr = prow + ((c8 ^ (row & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w0), "r"(w1), "r"(w2), "r"(w3)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * c8]), "r"(pk[4 * c8 + 1]),
+                     "r"(pk[4 * c8 + 2]), "r"(pk[4 * c8 + 3])
                      : "memory");
       }
       l = l * alpha + sum;

@@ -24,7 +24,8 @@ using namespace wenc_dev;
 
 constexpr int BM = wenc_host::kGemmBM;
 constexpr int BK = wenc_host::kGemmBK;
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;                // two warps per TMEM lane quadrant
+constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer warp, MMA warp, epilogue warps
 
 template <int BN>
 struct GemmCfg {
@@ -40,21 +41,19 @@ struct GemmCfg {
 __device__ __forceinline__ float gelu_erf(float z) { return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f)); }
 
 template <int EPI>
-__device__ __forceinline__ void epilogue_chunk(const uint32_t (&acc)[32], const float* __restrict__ bias,
-                                               const float* resid, void* out, size_t row_off, int col0) {
+__device__ __forceinline__ void epilogue_chunk(const uint32_t (&acc)[32], const float4 (&rr)[8],
+                                               const float* __restrict__ bias, void* out, size_t row_off, int col0) {
   const float4* b4 = reinterpret_cast<const float4*>(bias + col0);
   if constexpr (EPI == 2) {
-    const float4* r4 = reinterpret_cast<const float4*>(resid + row_off + col0);
     float4* o4 = reinterpret_cast<float4*>(static_cast<float*>(out) + row_off + col0);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const float4 bb = __ldg(b4 + j);
-      const float4 rr = r4[j];
       float4 v;
-      v.x = rr.x + (__uint_as_float(acc[4 * j + 0]) + bb.x);
-      v.y = rr.y + (__uint_as_float(acc[4 * j + 1]) + bb.y);
-      v.z = rr.z + (__uint_as_float(acc[4 * j + 2]) + bb.z);
-      v.w = rr.w + (__uint_as_float(acc[4 * j + 3]) + bb.w);
+      v.x = rr[j].x + (__uint_as_float(acc[4 * j + 0]) + bb.x);
+      v.y = rr[j].y + (__uint_as_float(acc[4 * j + 1]) + bb.y);
+      v.z = rr[j].z + (__uint_as_float(acc[4 * j + 2]) + bb.z);
+      v.w = rr[j].w + (__uint_as_float(acc[4 * j + 3]) + bb.w);
       o4[j] = v;
     }
   } else {
@@ -76,6 +75,13 @@ __device__ __forceinline__ void epilogue_chunk(const uint32_t (&acc)[32], const 
 #pragma unroll
     for (int q = 0; q < 4; ++q) o[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
   }
+}
+
+// Residual row segment of 32 fp32 values (128 bytes) into registers.
+__device__ __forceinline__ void load_resid(float4 (&rr)[8], const float* resid, size_t off) {
+  const float4* r4 = reinterpret_cast<const float4*>(resid + off);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) rr[j] = r4[j];
 }
 
 template <int BN, int EPI>
@@ -113,7 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 4);  // one arrival per epilogue warp
+      mbar_init(tempty_bar(a), kEpiWarps);  // one arrival per epilogue warp
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0u;
@@ -191,29 +197,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait_drain(drain_bar, 0);
   } else if (warp >= 2) {
     // ---------------- epilogue: TMEM -> registers -> global
-    const int quad = warp & 3;  // TMEM lane quadrant this warp may access
+    // Eight warps: warp w reads TMEM lane quadrant w % 4 (rows 32q..32q+31 of the tile) and
+    // one half of the tile's columns. Each thread owns one output row. For the residual
+    // epilogue the row's fp32 residual is loaded two 32-column chunks ahead, starting
+    // before the accumulator is ready, so that enough bytes are in flight to cover HBM
+    // latency; the TMEM buffer is released as soon as its last chunk has been read.
+    constexpr int CH = BN / 64;  // 32-column chunks per warp
+    const int quad = warp & 3;
+    const int col_half = (warp - 2) >> 2;
     const int row_in_tile = quad * 32 + lane;
     int local = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
-      if (!mbar_wait_warp(tfull_bar(acc), acc_phase, wc, 4)) break;
-      tc_fence_after();
       const int m0 = (tile / n_tiles) * BM;
       const int n0 = (tile % n_tiles) * BN;
       const int row = m0 + row_in_tile;
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
+      const bool live = row < M;
+      const int c0 = n0 + col_half * (BN / 2);
       const size_t row_off = static_cast<size_t>(row) * N;
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      float4 rb[2][8];
+      if constexpr (EPI == 2) {
+        if (live) {
+          load_resid(rb[0], resid, row_off + c0);
+          if (CH > 1) load_resid(rb[1], resid, row_off + c0 + 32);
+        }
+      }
+      if (!mbar_wait_warp(tfull_bar(acc), acc_phase, wc, 4)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN + col_half * (BN / 2);
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(taddr + c * 32, r);
         tmem_ld_wait();
-        if (row < M) epilogue_chunk<EPI>(r, bias, resid, out, row_off, n0 + c * 32);
+        if (c == CH - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty_bar(acc));
+        }
+        if (live) epilogue_chunk<EPI>(r, rb[c & 1], bias, out, row_off, c0 + c * 32);
+        if constexpr (EPI == 2) {
+          if (live && c + 2 < CH) load_resid(rb[c & 1], resid, row_off + c0 + (c + 2) * 32);
+        }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(acc));
     }
   }
 
