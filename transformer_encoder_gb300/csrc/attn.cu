@@ -7,12 +7,13 @@
 //
 // How (sm_103a): one CTA per (128-query tile, head, window), two CTAs per SM. Warp 0 streams
 // K/V tiles of 64 keys with TMA into a 3-deep ring; one thread of warp 1 issues
-// S = Q K^T (128 x 64 x 64) into TMEM and, once the softmax warps have written P, O += P V
-// (128 x 64 x 64, V read MN-major) into a TMEM accumulator. Warps 2-5 own one query row per
-// thread: they read S from TMEM, keep the running maximum and denominator in registers
-// (the online-softmax recurrence of VANILLA_ATTN, in base 2 with hd^-0.5*log2(e) folded in),
-// write P as bf16 into 128-byte-swizzled shared memory and, when the running maximum grows
-// by more than 2^8, rescale O in TMEM. No T x T score buffer exists.
+// S = Q K^T (128 x 64 x 64) into one of two TMEM score buffers and, once the softmax warps
+// have written P, O += P V (128 x 64 x 64, V read MN-major) into a TMEM accumulator; S[j+2]
+// is queued right behind PV[j]. Warps 2-5 own one query row per thread: they read S from
+// TMEM, keep the running maximum and denominator in registers (the online-softmax recurrence
+// of VANILLA_ATTN, in base 2 with hd^-0.5*log2(e) folded in), write P as bf16 into one of two
+// 128-byte-swizzled shared-memory buffers and, only when the running maximum grows by more
+// than 2^8, wait for the previous PV and rescale O in TMEM. No T x T score buffer exists.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -33,14 +34,14 @@ constexpr uint32_t Q_BYTES = BQ * HD * 2;    // 16 KB
 constexpr uint32_t P_BYTES = BQ * BKV * 2;   // 16 KB
 constexpr uint32_t KV_BYTES = BKV * HD * 2;  // 8 KB per K or V tile
 constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_P = OFF_Q + Q_BYTES;
-constexpr uint32_t OFF_K = OFF_P + P_BYTES;
+constexpr uint32_t OFF_P = OFF_Q + Q_BYTES;  // two P buffers
+constexpr uint32_t OFF_K = OFF_P + 2 * P_BYTES;
 constexpr uint32_t OFF_V = OFF_K + NST * KV_BYTES;
 constexpr uint32_t OFF_BARS = OFF_V + NST * KV_BYTES;
-// bars: q_full, kv_full[NST], kv_empty[NST], s_full, s_free, p_full, o_done, drain
-constexpr int NUM_BARS = 1 + 2 * NST + 5;
+// bars: q_full, kv_full[NST], kv_empty[NST], s_full[2], s_free[2], p_full[2], pv_done[2], drain
+constexpr int NUM_BARS = 1 + 2 * NST + 9;
 constexpr size_t SMEM = 1024 + OFF_BARS + NUM_BARS * 8 + 16;
-constexpr uint32_t TMEM_COLS = 128;  // S: columns 0..63, O: columns 64..127
+constexpr uint32_t TMEM_COLS = 256;  // S buffers: columns 0..63 and 64..127; O: 128..191
 // Grow the running maximum only when a tile's maximum exceeds it by more than this (log2
 // units); otherwise keep it, so p <= 2^8 and O is rescaled rarely. The result is unchanged:
 // numerator and denominator always use the same reference maximum.
@@ -58,11 +59,12 @@ __global__ void __launch_bounds__(kThreads, 2)
   const uint32_t q_full = bar0;
   auto kv_full = [&](int s) { return bar0 + 8u * (1 + s); };
   auto kv_empty = [&](int s) { return bar0 + 8u * (1 + NST + s); };
-  const uint32_t s_full = bar0 + 8u * (1 + 2 * NST);
-  const uint32_t s_free = s_full + 8u;
-  const uint32_t p_full = s_full + 16u;
-  const uint32_t o_done = s_full + 24u;
-  const uint32_t drain = s_full + 32u;
+  const uint32_t sb0 = bar0 + 8u * (1 + 2 * NST);
+  auto s_full = [&](int b) { return sb0 + 8u * b; };
+  auto s_free = [&](int b) { return sb0 + 16u + 8u * b; };
+  auto p_full = [&](int b) { return sb0 + 32u + 8u * b; };
+  auto pv_done = [&](int b) { return sb0 + 48u + 8u * b; };
+  const uint32_t drain = sb0 + 64u;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_BARS + NUM_BARS * 8);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   const WaitCtx wc{abort_flag, err};
@@ -80,10 +82,12 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_init(kv_full(s), 1);
       mbar_init(kv_empty(s), 1);
     }
-    mbar_init(s_full, 1);
-    mbar_init(s_free, 4);  // one arrival per softmax warp
-    mbar_init(p_full, 4);
-    mbar_init(o_done, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(s_full(i), 1);
+      mbar_init(s_free(i), 4);  // one arrival per softmax warp
+      mbar_init(p_full(i), 4);
+      mbar_init(pv_done(i), 1);
+    }
     mbar_init(drain, 1);
     *abort_flag = 0u;
     fence_barrier_init();
@@ -99,8 +103,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const uint32_t tS = tmem_base;
-  const uint32_t tO = tmem_base + 64;
+  auto tS = [&](int b) { return tmem_base + 64u * b; };
+  const uint32_t tO = tmem_base + 128;
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer
@@ -123,38 +127,37 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------- UMMA issuer
+    // Order on the tensor pipe: S0, S1, PV0, S2, PV1, S3, ... S[j+2] is queued right behind
+    // PV[j], so a score tile is always ready before the softmax warps ask for it.
     constexpr uint32_t idesc_s = idesc_bf16_f32(BQ, BKV, false);  // B = K tile, K-major
     constexpr uint32_t idesc_o = idesc_bf16_f32(BQ, HD, true);    // B = V tile, MN-major
-    bool ok = mbar_wait(q_full, 0, wc, 12) && mbar_wait(kv_full(0), 0, wc, 13);
-    if (ok) {
+    auto issue_s = [&](int j) -> bool {
+      const int st = j % NST;
+      if (!mbar_wait(kv_full(st), (j / NST) & 1, wc, 13)) return false;
+      if (j >= 2 && !mbar_wait(s_free(j & 1), ((j - 2) >> 1) & 1, wc, 14)) return false;
       tc_fence_after();
+      const uint32_t kb = sK + st * KV_BYTES;
 #pragma unroll
       for (int k = 0; k < HD / 16; ++k)
-        umma_bf16_ss(tS, sdesc_sw128(sQ + k * 32, 16, 1024), sdesc_sw128(sK + k * 32, 16, 1024), idesc_s, k > 0);
-      umma_commit(s_full);
-    }
+        umma_bf16_ss(tS(j & 1), sdesc_sw128(sQ + k * 32, 16, 1024), sdesc_sw128(kb + k * 32, 16, 1024), idesc_s,
+                     k > 0);
+      umma_commit(s_full(j & 1));
+      return true;
+    };
+    bool ok = mbar_wait(q_full, 0, wc, 12) && issue_s(0) && (n_kv < 2 || issue_s(1));
     for (int j = 0; ok && j < n_kv; ++j) {
       const int st = j % NST;
-      if (j + 1 < n_kv) {
-        const int st1 = (j + 1) % NST;
-        if (!mbar_wait(kv_full(st1), ((j + 1) / NST) & 1, wc, 14)) break;
-        if (!mbar_wait(s_free, j & 1, wc, 15)) break;
-        tc_fence_after();
-        const uint32_t kb = sK + st1 * KV_BYTES;
-#pragma unroll
-        for (int k = 0; k < HD / 16; ++k)
-          umma_bf16_ss(tS, sdesc_sw128(sQ + k * 32, 16, 1024), sdesc_sw128(kb + k * 32, 16, 1024), idesc_s, k > 0);
-        umma_commit(s_full);
-      }
-      if (!mbar_wait(p_full, j & 1, wc, 16)) break;
+      if (!mbar_wait(p_full(j & 1), (j >> 1) & 1, wc, 16)) break;
       tc_fence_after();
+      const uint32_t pb = sP + (j & 1) * P_BYTES;
       const uint32_t vb = sV + st * KV_BYTES;
 #pragma unroll
       for (int k = 0; k < BKV / 16; ++k)
-        umma_bf16_ss(tO, sdesc_sw128(sP + k * 32, 16, 1024), sdesc_sw128(vb + k * 2048, 1024, 1024), idesc_o,
+        umma_bf16_ss(tO, sdesc_sw128(pb + k * 32, 16, 1024), sdesc_sw128(vb + k * 2048, 1024, 1024), idesc_o,
                      (j > 0 || k > 0) ? 1u : 0u);
-      umma_commit(o_done);
+      umma_commit(pv_done(j & 1));
       umma_commit(kv_empty(st));
+      if (j + 2 < n_kv) ok = issue_s(j + 2);
     }
     umma_commit(drain);
     mbar_wait_drain(drain, 0);
@@ -167,15 +170,16 @@ __global__ void __launch_bounds__(kThreads, 2)
     float l = 0.0f;           // running denominator
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
-      if (!mbar_wait_warp(s_full, j & 1, wc, 17)) { ok = false; break; }
+      const int pb = j & 1;  // S buffer and P buffer of this tile
+      if (!mbar_wait_warp(s_full(pb), (j >> 1) & 1, wc, 17)) { ok = false; break; }
       tc_fence_after();
       uint32_t sr[2][32];
-      tmem_ld_32x32b_x32(tS + lane_off, sr[0]);
-      tmem_ld_32x32b_x32(tS + lane_off + 32, sr[1]);
+      tmem_ld_32x32b_x32(tS(pb) + lane_off, sr[0]);
+      tmem_ld_32x32b_x32(tS(pb) + lane_off + 32, sr[1]);
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(s_free);
+      if (lane == 0) mbar_arrive(s_free(pb));
 
       float sv[64];
 #pragma unroll
@@ -219,25 +223,26 @@ __global__ void __launch_bounds__(kThreads, 2)
       unpack_f32x2(sum2b, sb0, sb1);
       const float sum = (sa0 + sa1) + (sb0 + sb1);
 
-      if (j > 0) {
-        // PV of the previous tile must be complete: O is read below and P is overwritten.
-        if (!mbar_wait_warp(o_done, (j - 1) & 1, wc, 18)) { ok = false; break; }
+      if (j > 0 && __any_sync(0xffffffffu, m_new != m)) {
+        // The running maximum moved: O must hold every PV up to tile j-1 before it is rescaled.
+        if (!mbar_wait_warp(pv_done((j - 1) & 1), ((j - 1) >> 1) & 1, wc, 18)) { ok = false; break; }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, m_new != m)) {
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t o[32];
-            tmem_ld_32x32b_x32(tO + lane_off + half * 32, o);
-            tmem_ld_wait();
+        for (int half = 0; half < 2; ++half) {
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(tO + lane_off + half * 32, o);
+          tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-            tmem_st_32x32b_x32(tO + lane_off + half * 32, o);
-          }
-          tmem_st_wait();
+          for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+          tmem_st_32x32b_x32(tO + lane_off + half * 32, o);
         }
+        tmem_st_wait();
+      } else if (j >= 2) {
+        // P buffer pb was last read by PV[j-2].
+        if (!mbar_wait_warp(pv_done(pb), ((j - 2) >> 1) & 1, wc, 20)) { ok = false; break; }
       }
 
-      const uint32_t prow = sP + row * 128;
+      const uint32_t prow = sP + pb * P_BYTES + row * 128;
 #pragma unroll
       for (int c8 = 0; c8 < 8; ++c8) {
         const uint32_t addr = prow + ((c8 ^ (row & 7)) << 4);
@@ -250,9 +255,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) mbar_arrive(p_full(pb));
     }
-    if (ok && mbar_wait_warp(o_done, (n_kv - 1) & 1, wc, 19)) {
+    if (ok && mbar_wait_warp(pv_done((n_kv - 1) & 1), ((n_kv - 1) >> 1) & 1, wc, 19)) {
       tc_fence_after();
       const float inv_l = 1.0f / l;
       const int t = q0 + row;
