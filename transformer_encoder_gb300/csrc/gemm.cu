@@ -35,53 +35,89 @@ struct GemmCfg {
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TMEM_COLS = 2 * BN;  // two fp32 accumulators of BN columns
   static constexpr uint32_t NUM_BARS = 2 * STAGES + 5;
-  static constexpr size_t SMEM = 1024 /*align slack*/ + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
+  static constexpr uint32_t EPI_STAGE_BYTES = 32 * 32 * 4;  // one warp's 32 x 32 fp32 chunk
+  static constexpr uint32_t EPI_BYTES = kEpiWarps * EPI_STAGE_BYTES;
+  static constexpr size_t SMEM = 1024 /*align slack*/ + STAGES * STAGE_BYTES + EPI_BYTES + NUM_BARS * 8 + 16;
 };
 
-__device__ __forceinline__ float gelu_erf(float z) { return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f)); }
+// GELU(z) = z * Phi(z) = 0.5 z (1 + erf(z / sqrt(2))), with erf from the rational
+// approximation of Abramowitz & Stegun, Handbook of Mathematical Functions, formula 7.1.26:
+//   erf(x) = 1 - (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-x^2),  t = 1 / (1 + p x),  x >= 0,
+// |error| <= 1.5e-7, far below the bf16 rounding (2^-9 relative) of the fc1 output it feeds.
+// erf is odd, so erf(-x) = -erf(x). Two MUFU operations (reciprocal, exp2) and a handful of FMAs.
+__device__ __forceinline__ float gelu_erf(float z) {
+  const float x = fabsf(z) * 0.70710678118654752f;
+  float t;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t) : "f"(fmaf(0.3275911f, x, 1.0f)));
+  float poly = fmaf(t, 1.061405429f, -1.453152027f);
+  poly = fmaf(t, poly, 1.421413741f);
+  poly = fmaf(t, poly, -0.284496736f);
+  poly = fmaf(t, poly, 0.254829592f);
+  poly *= t;
+  const float e = ex2_approx(-1.4426950408889634f * x * x);  // exp(-x^2)
+  const float erf_abs = fmaf(-poly, e, 1.0f);
+  return 0.5f * z * (1.0f + copysignf(erf_abs, z));
+}
 
-template <int EPI>
-__device__ __forceinline__ void epilogue_chunk(const uint32_t (&acc)[32], const float4 (&rr)[8],
-                                               const float* __restrict__ bias, void* out, size_t row_off, int col0) {
-  const float4* b4 = reinterpret_cast<const float4*>(bias + col0);
-  if constexpr (EPI == 2) {
-    float4* o4 = reinterpret_cast<float4*>(static_cast<float*>(out) + row_off + col0);
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
+  return v;
+}
+
+// The epilogue moves each warp's 32-row x 32-column accumulator chunk through a 4 KB
+// shared-memory tile: thread r of the warp writes row r (as read from TMEM), then lane l
+// reads rows 4i + l/8, columns 4(l%8)..4(l%8)+3, so every global load and store of the warp
+// covers whole 128-byte row segments. 16-byte granules are XOR-swizzled by (row % 8), which
+// keeps both the row-wise writes and the segment-wise reads free of bank conflicts.
+__device__ __forceinline__ uint32_t stage_addr(uint32_t stage, int row, int granule) {
+  return stage + row * 128 + ((granule ^ (row & 7)) << 4);
+}
+
+// Residual values this lane will need for one chunk (rows grow0 + 4i + lane/8).
+__device__ __forceinline__ void load_resid(float4 (&rr)[8], const float* resid, int grow0, int M, int N, int col,
+                                           int lane) {
+  const int sub = lane >> 3, cl = lane & 7;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float4 bb = __ldg(b4 + j);
-      float4 v;
-      v.x = rr[j].x + (__uint_as_float(acc[4 * j + 0]) + bb.x);
-      v.y = rr[j].y + (__uint_as_float(acc[4 * j + 1]) + bb.y);
-      v.z = rr[j].z + (__uint_as_float(acc[4 * j + 2]) + bb.z);
-      v.w = rr[j].w + (__uint_as_float(acc[4 * j + 3]) + bb.w);
-      o4[j] = v;
-    }
-  } else {
-    uint32_t packed[16];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float4 bb = __ldg(b4 + j);
-      float v0 = __uint_as_float(acc[4 * j + 0]) + bb.x;
-      float v1 = __uint_as_float(acc[4 * j + 1]) + bb.y;
-      float v2 = __uint_as_float(acc[4 * j + 2]) + bb.z;
-      float v3 = __uint_as_float(acc[4 * j + 3]) + bb.w;
-      if constexpr (EPI == 1) {
-        v0 = gelu_erf(v0); v1 = gelu_erf(v1); v2 = gelu_erf(v2); v3 = gelu_erf(v3);
-      }
-      packed[2 * j] = pack_bf16x2(v0, v1);
-      packed[2 * j + 1] = pack_bf16x2(v2, v3);
-    }
-    uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + row_off + col0);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) o[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+  for (int i = 0; i < 8; ++i) {
+    const int grow = grow0 + 4 * i + sub;
+    if (grow < M) rr[i] = *reinterpret_cast<const float4*>(resid + static_cast<size_t>(grow) * N + col + 4 * cl);
   }
 }
 
-// Residual row segment of 32 fp32 values (128 bytes) into registers.
-__device__ __forceinline__ void load_resid(float4 (&rr)[8], const float* resid, size_t off) {
-  const float4* r4 = reinterpret_cast<const float4*>(resid + off);
+template <int EPI>
+__device__ __forceinline__ void epilogue_chunk(const uint32_t (&acc)[32], uint32_t stage, int lane, int grow0, int M,
+                                               int N, int col, const float* __restrict__ bias,
+                                               const float4 (&rr)[8], void* out) {
 #pragma unroll
-  for (int j = 0; j < 8; ++j) rr[j] = r4[j];
+  for (int q = 0; q < 8; ++q)
+    st_shared_v4(stage_addr(stage, lane, q), acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+  __syncwarp();
+  const int sub = lane >> 3, cl = lane & 7;
+  const float4 bb = __ldg(reinterpret_cast<const float4*>(bias + col) + cl);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = 4 * i + sub;
+    const float4 a = ld_shared_f4(stage_addr(stage, r, cl));
+    const int grow = grow0 + r;
+    if (grow < M) {
+      const size_t off = static_cast<size_t>(grow) * N + col + 4 * cl;
+      float4 v = make_float4(a.x + bb.x, a.y + bb.y, a.z + bb.z, a.w + bb.w);
+      if constexpr (EPI == 2) {
+        v = make_float4(rr[i].x + v.x, rr[i].y + v.y, rr[i].z + v.z, rr[i].w + v.w);
+        *reinterpret_cast<float4*>(static_cast<float*>(out) + off) = v;
+      } else {
+        if constexpr (EPI == 1) {
+          v.x = gelu_erf(v.x); v.y = gelu_erf(v.y); v.z = gelu_erf(v.z); v.w = gelu_erf(v.w);
+        }
+        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + off) = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+      }
+    }
+  }
+  __syncwarp();  // the stage is rewritten by the next chunk
 }
 
 template <int BN, int EPI>
@@ -94,7 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sA = smem_u32(smem);
   const uint32_t sB = sA + STAGES * C::A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES + C::EPI_BYTES);
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
@@ -196,33 +232,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     umma_commit(drain_bar);
     mbar_wait_drain(drain_bar, 0);
   } else if (warp >= 2) {
-    // ---------------- epilogue: TMEM -> registers -> global
+    // ---------------- epilogue: TMEM -> registers -> shared -> global
     // Eight warps: warp w reads TMEM lane quadrant w % 4 (rows 32q..32q+31 of the tile) and
-    // one half of the tile's columns. Each thread owns one output row. For the residual
-    // epilogue the row's fp32 residual is loaded two 32-column chunks ahead, starting
-    // before the accumulator is ready, so that enough bytes are in flight to cover HBM
-    // latency; the TMEM buffer is released as soon as its last chunk has been read.
+    // one half of the tile's columns, 32 columns at a time (see epilogue_chunk). For the
+    // residual epilogue each lane keeps two chunks of residual loads in flight, continuing into
+    // the next tile (the first tile's before its accumulator is ready). The TMEM buffer is
+    // released as soon as its last chunk has been read.
     constexpr int CH = BN / 64;  // 32-column chunks per warp
     const int quad = warp & 3;
     const int col_half = (warp - 2) >> 2;
-    const int row_in_tile = quad * 32 + lane;
+    const uint32_t stage = smem_u32(smem + STAGES * C::STAGE_BYTES) + (warp - 2) * C::EPI_STAGE_BYTES;
+    auto row0_of = [&](int t) { return (t / n_tiles) * BM + quad * 32; };
+    auto col_of = [&](int t) { return (t % n_tiles) * BN + col_half * (BN / 2); };
+    float4 rb[2][8];
+    if constexpr (EPI == 2) {
+      if (blockIdx.x < num_tiles) {
+        load_resid(rb[0], resid, row0_of(blockIdx.x), M, N, col_of(blockIdx.x), lane);
+        if (CH > 1) load_resid(rb[1], resid, row0_of(blockIdx.x), M, N, col_of(blockIdx.x) + 32, lane);
+      }
+    }
     int local = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
-      const int m0 = (tile / n_tiles) * BM;
-      const int n0 = (tile % n_tiles) * BN;
-      const int row = m0 + row_in_tile;
-      const bool live = row < M;
-      const int c0 = n0 + col_half * (BN / 2);
-      const size_t row_off = static_cast<size_t>(row) * N;
-      float4 rb[2][8];
-      if constexpr (EPI == 2) {
-        if (live) {
-          load_resid(rb[0], resid, row_off + c0);
-          if (CH > 1) load_resid(rb[1], resid, row_off + c0 + 32);
-        }
-      }
+      const int grow0 = row0_of(tile);
+      const int c0 = col_of(tile);
+      const int next = tile + gridDim.x;
       if (!mbar_wait_warp(tfull_bar(acc), acc_phase, wc, 4)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN + col_half * (BN / 2);
@@ -236,9 +271,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(tempty_bar(acc));
         }
-        if (live) epilogue_chunk<EPI>(r, rb[c & 1], bias, out, row_off, c0 + c * 32);
+        epilogue_chunk<EPI>(r, stage, lane, grow0, M, N, c0 + c * 32, bias, rb[c & 1], out);
         if constexpr (EPI == 2) {
-          if (live && c + 2 < CH) load_resid(rb[c & 1], resid, row_off + c0 + (c + 2) * 32);
+          if (c + 2 < CH) {
+            load_resid(rb[c & 1], resid, grow0, M, N, c0 + (c + 2) * 32, lane);
+          } else if (next < num_tiles) {
+            load_resid(rb[c & 1], resid, row0_of(next), M, N, col_of(next) + (c + 2 - CH) * 32, lane);
+          }
         }
       }
     }
