@@ -43,6 +43,48 @@ def load_peaks():
     return dict(PEAKS_FALLBACK), "fallback"
 
 
+def kernel_source_hash() -> str:
+    """sha256 over the CUDA sources and headers of libwenc (identifies the profiled build)."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "transformer_encoder_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            h.update(name.encode())
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
+    with open(os.path.join(ROOT, "include", "wenc.h"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()
+
+
+def load_traffic():
+    """DRAM bytes per launch measured by ncu (profiles/traffic.json), or None once the kernel
+    sources differ from the ones that were profiled."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    return d if d.get("source_sha256") == kernel_source_hash() else None
+
+
+def combine_rank_timings(ms_total: float, ms_e2e: float, world: int, device="cuda"):
+    """The slowest rank sets the job's time: max over ranks of both timed regions."""
+    if world == 1:
+        return ms_total, ms_e2e
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms_total, ms_e2e], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t[0]), float(t[1])
+
+
+def job_throughput(windows_per_rank: int, world: int, steps: int, ms_total: float) -> float:
+    """Windows per second of the whole job: every rank's windows over the slowest rank's time."""
+    return windows_per_rank * world * steps / (ms_total / 1e3)
+
+
 def dist_env():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
 
@@ -279,15 +321,11 @@ def run_wenc(args, w):
     barrier()
     ms_e2e = e_start.elapsed_time(e_stop)
 
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([ms_total, ms_e2e], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total, ms_e2e = tt.tolist()
+    ms_total, ms_e2e = combine_rank_timings(ms_total, ms_e2e, world)
 
     ms_step = ms_total / args.steps
     windows = w.batch * world
-    value = windows * args.steps / (ms_total / 1e3)
+    value = job_throughput(w.batch, world, args.steps, ms_total)
     flops_step = w.flops()
     tflops = flops_step * world / (ms_step / 1e3) / 1e12
 
@@ -315,9 +353,19 @@ def run_wenc(args, w):
     g_flops_per_launch = sum(gemm_flops[k] * per_kind[k][1] for k in gemm_flops if k in per_kind) / g_n
     g_achieved = g_flops_per_launch / (g_ms / g_n / 1e3) / 1e12
     peak = peaks.get("bf16_tflops_sustained", PEAKS_FALLBACK["bf16_tflops_sustained"])
+    traffic = load_traffic() if w.name in ("large_stack", "large_block") else None
+    g_traffic = None
+    if traffic is not None:
+        per = traffic["bytes_per_launch"]
+        for name in kern:
+            if name in per:
+                kern[name]["traffic_bytes"] = per[name]
+        if all(k in per for k in gemm_flops):
+            g_traffic = sum(per[k] * per_kind[k][1] for k in gemm_flops) / g_n
     roofline = {"kernel": "gemm_tc_kernel (QKV, out-proj, fc1, fc2 launches)", "bound": "tensor",
                 "achieved": g_achieved, "peak": peak, "unit": "TFLOP/s", "frac": g_achieved / peak,
-                "peak_source": f"bf16_tflops_sustained, {peak_src}", "traffic": None}
+                "peak_source": f"bf16_tflops_sustained, {peak_src}", "traffic": g_traffic,
+                "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)"}
 
     line = {
         "metric": METRIC, "value": value, "unit": "windows/s", "n_gpus": world, "steps": args.steps,
