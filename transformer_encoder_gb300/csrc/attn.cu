@@ -5,15 +5,22 @@
 //   s_j = (q_i . k_j) * hd^-0.5 over all T keys,  p = softmax(s),  o_i = sum_j p_j v_j.
 // No mask beyond the window's own length, no positional term.
 //
-// How (sm_103a): one CTA per (128-query tile, head, window), two CTAs per SM. Warp 0 streams
-// K/V tiles of 64 keys with TMA into a 3-deep ring; one thread of warp 1 issues
-// S = Q K^T (128 x 64 x 64) into one of two TMEM score buffers and, once the softmax warps
-// have written P, O += P V (128 x 64 x 64, V read MN-major) into a TMEM accumulator; S[j+2]
-// is queued right behind PV[j]. Warps 2-5 own one query row per thread: they read S from
-// TMEM, keep the running maximum and denominator in registers (the online-softmax recurrence
-// of VANILLA_ATTN, in base 2 with hd^-0.5*log2(e) folded in), write P as bf16 into one of two
-// 128-byte-swizzled shared-memory buffers and, only when the running maximum grows by more
-// than 2^8, wait for the previous PV and rescale O in TMEM. No T x T score buffer exists.
+// How (sm_103a). One CTA per (256 queries, head, window), one CTA per SM. The 256 queries are
+// two 128-row tiles A and B that share every K/V tile:
+//  - warp 0 streams Q_A, Q_B once and K, V tiles of 128 keys (TMA, 128-byte swizzle) through
+//    rings of their own, in the order the tensor pipe consumes them;
+//  - one thread of warp 1 issues S_A = Q_A K_j^T and S_B = Q_B K_j^T (M128 N128 K64, into TMEM)
+//    as soon as the scores of tile j-1 have been read; one thread each of warps 2 and 3 issues
+//    O_A += P_A V_j and O_B += P_B V_j (M128 N64, V read MN-major, O accumulated in TMEM) once P
+//    of tile j is written (one issuing thread cannot keep the tensor pipe fed with N = 64 MMAs);
+//  - warps 4-7 (tile A) and 8-11 (tile B) own one query row per thread: they read the row's 128
+//    scores from TMEM, keep the running maximum and denominator in registers (the online-softmax
+//    recurrence of VANILLA_ATTN, in base 2 with hd^-0.5*log2(e) folded in), write P as bf16 into
+//    128-byte-swizzled shared memory and rescale O in TMEM when the running maximum moves by more
+//    than 2^8. The two tiles take turns on the exponentials (ping-pong), so one tile's exps run
+//    while the other tile loads scores, stores P or waits, and the tensor pipe runs the other
+//    tile's products meanwhile. No T x T score buffer exists.
+// Key tiles of 128 make the S products full-rate (N = 128); the PV products have N = hd = 64.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -24,30 +31,33 @@ namespace {
 
 using namespace wenc_dev;
 
-constexpr int BQ = wenc_host::kAttnBQ;    // query rows per CTA
+constexpr int BQ = wenc_host::kAttnBQ;    // query rows per tile (two tiles per CTA)
 constexpr int BKV = wenc_host::kAttnBKV;  // keys per tile
 constexpr int HD = 64;
-constexpr int NST = 3;  // K/V ring depth
-constexpr int kThreads = 192;
+constexpr int NK = 3;                     // K ring depth
+constexpr int NV = 3;                     // V ring depth
+constexpr int kThreads = 384;             // producer, 3 MMA issuers, 2 softmax warpgroups
 
-constexpr uint32_t Q_BYTES = BQ * HD * 2;    // 16 KB
-constexpr uint32_t P_BYTES = BQ * BKV * 2;   // 16 KB
-constexpr uint32_t KV_BYTES = BKV * HD * 2;  // 8 KB per K or V tile
-constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_P = OFF_Q + Q_BYTES;  // two P buffers
+constexpr uint32_t Q_BYTES = BQ * HD * 2;           // 16 KB per query tile
+constexpr uint32_t P_HALF = BQ * 64 * 2;            // 16 KB: 128 rows x 64 keys, one swizzle-atom column
+constexpr uint32_t P_BYTES = 2 * P_HALF;            // 32 KB per query tile
+constexpr uint32_t KV_BYTES = BKV * HD * 2;         // 16 KB per K or V tile
+constexpr uint32_t OFF_Q = 0;                       // Q_A, Q_B
+constexpr uint32_t OFF_P = OFF_Q + 2 * Q_BYTES;     // P_A, P_B
 constexpr uint32_t OFF_K = OFF_P + 2 * P_BYTES;
-constexpr uint32_t OFF_V = OFF_K + NST * KV_BYTES;
-constexpr uint32_t OFF_BARS = OFF_V + NST * KV_BYTES;
-// bars: q_full, kv_full[NST], kv_empty[NST], s_full[2], s_free[2], p_full[2], pv_done[2], drain
-constexpr int NUM_BARS = 1 + 2 * NST + 9;
+constexpr uint32_t OFF_V = OFF_K + NK * KV_BYTES;
+constexpr uint32_t OFF_BARS = OFF_V + NV * KV_BYTES;
+// bars: q_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], and per query tile t:
+// s_full[t], s_free[t], p_full[t], pv_done[t], turn[t]; drain
+constexpr int NUM_BARS = 1 + 2 * NK + 2 * NV + 10 + 1;
 constexpr size_t SMEM = 1024 + OFF_BARS + NUM_BARS * 8 + 16;
-constexpr uint32_t TMEM_COLS = 256;  // S buffers: columns 0..63 and 64..127; O: 128..191
+constexpr uint32_t TMEM_COLS = 512;  // S_A 0..127, S_B 128..255, O_A 256..319, O_B 320..383
 // Grow the running maximum only when a tile's maximum exceeds it by more than this (log2
 // units); otherwise keep it, so p <= 2^8 and O is rescaled rarely. The result is unchanged:
 // numerator and denominator always use the same reference maximum.
 constexpr float kRescaleThreshold = 8.0f;
 
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, int q_col0, int k_col0, int v_col0,
                     uint16_t* __restrict__ out, int out_stride, int T, float scale_log2, uint32_t* err) {
@@ -57,38 +67,46 @@ __global__ void __launch_bounds__(kThreads, 2)
   const uint32_t sQ = s0 + OFF_Q, sP = s0 + OFF_P, sK = s0 + OFF_K, sV = s0 + OFF_V;
   const uint32_t bar0 = s0 + OFF_BARS;
   const uint32_t q_full = bar0;
-  auto kv_full = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto kv_empty = [&](int s) { return bar0 + 8u * (1 + NST + s); };
-  const uint32_t sb0 = bar0 + 8u * (1 + 2 * NST);
-  auto s_full = [&](int b) { return sb0 + 8u * b; };
-  auto s_free = [&](int b) { return sb0 + 16u + 8u * b; };
-  auto p_full = [&](int b) { return sb0 + 32u + 8u * b; };
-  auto pv_done = [&](int b) { return sb0 + 48u + 8u * b; };
-  const uint32_t drain = sb0 + 64u;
+  auto k_full = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto k_empty = [&](int s) { return bar0 + 8u * (1 + NK + s); };
+  auto v_full = [&](int s) { return bar0 + 8u * (1 + 2 * NK + s); };
+  auto v_empty = [&](int s) { return bar0 + 8u * (1 + 2 * NK + NV + s); };
+  const uint32_t tb0 = bar0 + 8u * (1 + 2 * NK + 2 * NV);
+  auto s_full = [&](int t) { return tb0 + 8u * t; };
+  auto s_free = [&](int t) { return tb0 + 16u + 8u * t; };
+  auto p_full = [&](int t) { return tb0 + 32u + 8u * t; };
+  auto pv_done = [&](int t) { return tb0 + 48u + 8u * t; };
+  auto turn = [&](int t) { return tb0 + 64u + 8u * t; };  // tile t may run its exponentials
+  const uint32_t drain = tb0 + 80u;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_BARS + NUM_BARS * 8);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   const WaitCtx wc{abort_flag, err};
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int q0 = blockIdx.x * BQ;
+  const int q0 = blockIdx.x * 2 * BQ;
   const int h = blockIdx.y;
   const int b = blockIdx.z;
   const int n_kv = (T + BKV - 1) / BKV;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < NST; ++s) {
-      mbar_init(kv_full(s), 1);
-      mbar_init(kv_empty(s), 1);
+    for (int s = 0; s < NK; ++s) {
+      mbar_init(k_full(s), 1);
+      mbar_init(k_empty(s), 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(s_full(i), 1);
-      mbar_init(s_free(i), 4);  // one arrival per softmax warp
-      mbar_init(p_full(i), 4);
-      mbar_init(pv_done(i), 1);
+    for (int s = 0; s < NV; ++s) {
+      mbar_init(v_full(s), 1);
+      mbar_init(v_empty(s), 2);  // released by both PV issuers
     }
-    mbar_init(drain, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(s_full(t), 1);
+      mbar_init(s_free(t), 4);  // one arrival per softmax warp of the tile
+      mbar_init(p_full(t), 4);
+      mbar_init(pv_done(t), 1);
+      mbar_init(turn(t), 4);  // the other tile's four softmax warps pass the turn
+    }
+    mbar_init(drain, 3);  // one commit per MMA-issuing thread
     *abort_flag = 0u;
     fence_barrier_init();
     tma_prefetch_desc(&tq);
@@ -103,114 +121,148 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  auto tS = [&](int b) { return tmem_base + 64u * b; };
-  const uint32_t tO = tmem_base + 128;
+  auto tS = [&](int t) { return tmem_base + 128u * t; };
+  auto tO = [&](int t) { return tmem_base + 256u + 64u * t; };
 
   if (warp == 0 && lane == 0) {
-    // ---------------- TMA producer
-    mbar_arrive_expect_tx(q_full, Q_BYTES);
+    // ---------------- TMA producer: Q_A, Q_B; then K0, then (K[j], V[j-1]) for j >= 1, then V[n-1]
+    mbar_arrive_expect_tx(q_full, 2 * Q_BYTES);
     tma_load_3d(sQ, &tq, q_full, q_col0 + h * HD, q0, b);
-    int issued = 0;
-    for (int j = 0; j < n_kv; ++j) {
-      const int st = j % NST;
-      const uint32_t ph = (j / NST) & 1;
-      if (!mbar_wait(kv_empty(st), ph ^ 1u, wc, 11)) break;
-      mbar_arrive_expect_tx(kv_full(st), 2 * KV_BYTES);
-      tma_load_3d(sK + st * KV_BYTES, &tk, kv_full(st), k_col0 + h * HD, j * BKV, b);
-      tma_load_3d(sV + st * KV_BYTES, &tv, kv_full(st), v_col0 + h * HD, j * BKV, b);
-      issued = j + 1;
+    tma_load_3d(sQ + Q_BYTES, &tq, q_full, q_col0 + h * HD, q0 + BQ, b);
+    int k_issued = 0, v_issued = 0;
+    auto load_k = [&](int j) -> bool {
+      const int st = j % NK;
+      if (!mbar_wait(k_empty(st), ((j / NK) & 1) ^ 1u, wc, 11)) return false;
+      mbar_arrive_expect_tx(k_full(st), KV_BYTES);
+      tma_load_3d(sK + st * KV_BYTES, &tk, k_full(st), k_col0 + h * HD, j * BKV, b);
+      k_issued = j + 1;
+      return true;
+    };
+    auto load_v = [&](int j) -> bool {
+      const int st = j % NV;
+      if (!mbar_wait(v_empty(st), ((j / NV) & 1) ^ 1u, wc, 10)) return false;
+      mbar_arrive_expect_tx(v_full(st), KV_BYTES);
+      tma_load_3d(sV + st * KV_BYTES, &tv, v_full(st), v_col0 + h * HD, j * BKV, b);
+      v_issued = j + 1;
+      return true;
+    };
+    bool ok = true;
+    for (int j = 0; ok && j <= n_kv; ++j) {
+      if (j < n_kv) ok = load_k(j);
+      if (ok && j >= 1) ok = load_v(j - 1);
     }
     if (*abort_flag) {
       // Error path: let the copies already issued land before the CTA exits.
       mbar_wait_drain(q_full, 0);
-      for (int j = (issued > NST ? issued - NST : 0); j < issued; ++j) mbar_wait_drain(kv_full(j % NST), (j / NST) & 1);
+      for (int j = (k_issued > NK ? k_issued - NK : 0); j < k_issued; ++j) mbar_wait_drain(k_full(j % NK), (j / NK) & 1);
+      for (int j = (v_issued > NV ? v_issued - NV : 0); j < v_issued; ++j) mbar_wait_drain(v_full(j % NV), (j / NV) & 1);
     }
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- UMMA issuer
-    // Order on the tensor pipe: S0, S1, PV0, S2, PV1, S3, ... S[j+2] is queued right behind
-    // PV[j], so a score tile is always ready before the softmax warps ask for it.
-    constexpr uint32_t idesc_s = idesc_bf16_f32(BQ, BKV, false);  // B = K tile, K-major
-    constexpr uint32_t idesc_o = idesc_bf16_f32(BQ, HD, true);    // B = V tile, MN-major
-    auto issue_s = [&](int j) -> bool {
-      const int st = j % NST;
-      if (!mbar_wait(kv_full(st), (j / NST) & 1, wc, 13)) return false;
-      if (j >= 2 && !mbar_wait(s_free(j & 1), ((j - 2) >> 1) & 1, wc, 14)) return false;
-      tc_fence_after();
-      const uint32_t kb = sK + st * KV_BYTES;
+  } else if (warp >= 1 && warp <= 3 && lane == 0) {
+    // ---------------- UMMA issuers. A single thread cannot issue MMAs fast enough to keep the
+    // tensor pipe busy with N = 64 products, so three threads share the work: warp 1 issues
+    // S_A = Q_A K_j^T and S_B = Q_B K_j^T as soon as the scores of tile j-1 have been read;
+    // warps 2 and 3 issue O_A += P_A V_j and O_B += P_B V_j once P of tile j is written.
+    // Descriptors are built once per operand tile; a K step of 16 elements advances the start
+    // address by 32 bytes (K-major, inside the 128-byte swizzle row: +2 in the >>4 field) or by
+    // 16 rows of 128 bytes (the MN-major V tile: +128).
+    bool ok = mbar_wait(q_full, 0, wc, 12);
+    if (warp == 1) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(BQ, BKV, false);  // B = K tile, K-major, N = 128
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int st = j % NK;
+        if (!mbar_wait(k_full(st), (j / NK) & 1, wc, 13)) break;
+        const uint64_t kdesc = sdesc_sw128(sK + st * KV_BYTES, 16, 1024);
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (j >= 1 && !mbar_wait(s_free(t), (j - 1) & 1, wc, 14)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t qdesc = sdesc_sw128(sQ + t * Q_BYTES, 16, 1024);
 #pragma unroll
-      for (int k = 0; k < HD / 16; ++k)
-        umma_bf16_ss(tS(j & 1), sdesc_sw128(sQ + k * 32, 16, 1024), sdesc_sw128(kb + k * 32, 16, 1024), idesc_s,
-                     k > 0);
-      umma_commit(s_full(j & 1));
-      return true;
-    };
-    bool ok = mbar_wait(q_full, 0, wc, 12) && issue_s(0) && (n_kv < 2 || issue_s(1));
-    for (int j = 0; ok && j < n_kv; ++j) {
-      const int st = j % NST;
-      if (!mbar_wait(p_full(j & 1), (j >> 1) & 1, wc, 16)) break;
-      tc_fence_after();
-      const uint32_t pb = sP + (j & 1) * P_BYTES;
-      const uint32_t vb = sV + st * KV_BYTES;
+          for (int k = 0; k < HD / 16; ++k) umma_bf16_ss(tS(t), qdesc + k * 2, kdesc + k * 2, idesc_s, k > 0);
+          umma_commit(s_full(t));
+        }
+        if (ok) umma_commit(k_empty(st));
+      }
+    } else {
+      constexpr uint32_t idesc_o = idesc_bf16_f32(BQ, HD, true);  // B = V tile, MN-major, N = 64
+      const int t = warp - 2;
+      const uint64_t pdesc = sdesc_sw128(sP + t * P_BYTES, 16, 1024);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int st = j % NV;
+        if (!mbar_wait(v_full(st), (j / NV) & 1, wc, 15)) break;
+        if (!mbar_wait(p_full(t), j & 1, wc, 16)) break;
+        tc_fence_after();
+        const uint64_t vdesc = sdesc_sw128(sV + st * KV_BYTES, 1024, 1024);
 #pragma unroll
-      for (int k = 0; k < BKV / 16; ++k)
-        umma_bf16_ss(tO, sdesc_sw128(pb + k * 32, 16, 1024), sdesc_sw128(vb + k * 2048, 1024, 1024), idesc_o,
-                     (j > 0 || k > 0) ? 1u : 0u);
-      umma_commit(pv_done(j & 1));
-      umma_commit(kv_empty(st));
-      if (j + 2 < n_kv) ok = issue_s(j + 2);
+        for (int k = 0; k < BKV / 16; ++k)
+          umma_bf16_ss(tO(t), pdesc + (k >> 2) * (P_HALF >> 4) + (k & 3) * 2, vdesc + k * 128, idesc_o,
+                       (j > 0 || k > 0) ? 1u : 0u);
+        umma_commit(pv_done(t));
+        umma_commit(v_empty(st));
+      }
     }
+    // Every MMA this thread issued completes before TMEM is released.
     umma_commit(drain);
     mbar_wait_drain(drain, 0);
-  } else if (warp >= 2) {
+  } else if (warp >= 4) {
     // ---------------- softmax / correction / output: one query row per thread
+    const int t = (warp - 4) >> 2;  // query tile of this warpgroup
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t prow = sP + t * P_BYTES + row * 128;
     float m = -CUDART_INF_F;  // running maximum, in units of scale_log2
     float l = 0.0f;           // running denominator
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
-      const int pb = j & 1;  // S buffer and P buffer of this tile
-      if (!mbar_wait_warp(s_full(pb), (j >> 1) & 1, wc, 17)) { ok = false; break; }
+      if (!mbar_wait_warp(s_full(t), j & 1, wc, 17)) { ok = false; break; }
       tc_fence_after();
-      uint32_t sr[2][32];
-      tmem_ld_32x32b_x32(tS(pb) + lane_off, sr[0]);
-      tmem_ld_32x32b_x32(tS(pb) + lane_off + 32, sr[1]);
-      tmem_ld_wait();
+      float sv[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tS(t) + lane_off + c * 32, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) sv[c * 32 + e] = __uint_as_float(r[e]);
+      }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(s_free(pb));
+      if (lane == 0) mbar_arrive(s_free(t));  // the MMA may overwrite S with the next tile
 
-      float sv[64];
-#pragma unroll
-      for (int c = 0; c < 64; ++c) sv[c] = __uint_as_float(sr[c >> 5][c & 31]);
       const int valid = T - j * BKV;  // keys of this tile inside the window
       if (valid < BKV) {              // only a window's last tile can be partial (warp-uniform)
 #pragma unroll
-        for (int c = 0; c < 64; ++c) sv[c] = (c < valid) ? sv[c] : -CUDART_INF_F;
+        for (int c = 0; c < 128; ++c) sv[c] = (c < valid) ? sv[c] : -CUDART_INF_F;
       }
-      // Row maximum: four independent chains of three-input max.
-      float mc[4];
+      // Row maximum: eight independent chains of three-input max.
+      float mc[8];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < 8; ++k) {
         float a = fmax3(sv[16 * k], sv[16 * k + 1], sv[16 * k + 2]);
 #pragma unroll
         for (int e = 3; e < 15; e += 2) a = fmax3(a, sv[16 * k + e], sv[16 * k + e + 1]);
         mc[k] = fmaxf(a, sv[16 * k + 15]);
       }
-      const float mx = fmaxf(fmax3(mc[0], mc[1], mc[2]), mc[3]);
+      const float mx = fmaxf(fmax3(mc[0], mc[1], mc[2]), fmax3(fmax3(mc[3], mc[4], mc[5]), mc[6], mc[7]));
       const float mx_s = mx * scale_log2;
       const float m_new = (mx_s > m + kRescaleThreshold) ? mx_s : m;
       const float alpha = ex2_approx(m - m_new);  // 0 on the first tile (m = -inf)
 
-      // p = 2^(s * scale_log2 - m_new): packed fp32x2 FMA for the argument, packed adds for
-      // the row sum; P is packed to bf16 pairs before waiting on the previous PV product.
+      // Ping-pong: the two tiles take turns on the exponentials (MUFU), so that one tile's
+      // exponentials overlap the other tile's loads, stores and waits instead of contending.
+      // Tile A's turn j follows tile B's exponentials of tile j-1; tile B's follows A's of j.
+      if (t == 1 || j > 0) {
+        if (!mbar_wait_warp(turn(t), (t == 0 ? j - 1 : j) & 1, wc, 21)) { ok = false; break; }
+      }
+
+      // p = 2^(s * scale_log2 - m_new): packed fp32x2 FMA for the argument, packed adds for the
+      // row sum; P is packed to bf16 pairs before waiting on the previous PV product.
       const uint64_t c2 = pack_f32x2(scale_log2, scale_log2);
       const uint64_t nm2 = pack_f32x2(-m_new, -m_new);
       uint64_t sum2a = pack_f32x2(0.0f, 0.0f), sum2b = sum2a;
-      uint32_t pk[32];
+      uint32_t pk[64];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
+      for (int i = 0; i < 64; ++i) {
         float a0, a1;
         unpack_f32x2(fma_f32x2(pack_f32x2(sv[2 * i], sv[2 * i + 1]), c2, nm2), a0, a1);
         const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
@@ -222,30 +274,31 @@ __global__ void __launch_bounds__(kThreads, 2)
       unpack_f32x2(sum2a, sa0, sa1);
       unpack_f32x2(sum2b, sb0, sb1);
       const float sum = (sa0 + sa1) + (sb0 + sb1);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(turn(1 - t));
 
-      if (j > 0 && __any_sync(0xffffffffu, m_new != m)) {
-        // The running maximum moved: O must hold every PV up to tile j-1 before it is rescaled.
-        if (!mbar_wait_warp(pv_done((j - 1) & 1), ((j - 1) >> 1) & 1, wc, 18)) { ok = false; break; }
+      if (j > 0) {
+        // PV[j-1] must be complete: P is overwritten below and O may be rescaled.
+        if (!mbar_wait_warp(pv_done(t), (j - 1) & 1, wc, 18)) { ok = false; break; }
         tc_fence_after();
+        if (__any_sync(0xffffffffu, m_new != m)) {
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t o[32];
-          tmem_ld_32x32b_x32(tO + lane_off + half * 32, o);
-          tmem_ld_wait();
+          for (int half = 0; half < 2; ++half) {
+            uint32_t o[32];
+            tmem_ld_32x32b_x32(tO(t) + lane_off + half * 32, o);
+            tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-          tmem_st_32x32b_x32(tO + lane_off + half * 32, o);
+            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+            tmem_st_32x32b_x32(tO(t) + lane_off + half * 32, o);
+          }
+          tmem_st_wait();
         }
-        tmem_st_wait();
-      } else if (j >= 2) {
-        // P buffer pb was last read by PV[j-2].
-        if (!mbar_wait_warp(pv_done(pb), ((j - 2) >> 1) & 1, wc, 20)) { ok = false; break; }
       }
 
-      const uint32_t prow = sP + pb * P_BYTES + row * 128;
+      // P row (128 keys) as two 64-key halves, each a K-major 128-byte-swizzled 128 x 64 tile.
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
-        const uint32_t addr = prow + ((c8 ^ (row & 7)) << 4);
+      for (int c8 = 0; c8 < 16; ++c8) {
+        const uint32_t addr = prow + (c8 >> 3) * P_HALF + (((c8 & 7) ^ (row & 7)) << 4);
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * c8]), "r"(pk[4 * c8 + 1]),
                      "r"(pk[4 * c8 + 2]), "r"(pk[4 * c8 + 3])
                      : "memory");
@@ -255,19 +308,19 @@ __global__ void __launch_bounds__(kThreads, 2)
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full(pb));
+      if (lane == 0) mbar_arrive(p_full(t));
     }
-    if (ok && mbar_wait_warp(pv_done((n_kv - 1) & 1), ((n_kv - 1) >> 1) & 1, wc, 19)) {
+    if (ok && mbar_wait_warp(pv_done(t), (n_kv - 1) & 1, wc, 19)) {
       tc_fence_after();
       const float inv_l = 1.0f / l;
-      const int t = q0 + row;
-      uint16_t* dst = out + (static_cast<size_t>(b) * T + t) * out_stride + h * HD;
+      const int tq_row = q0 + t * BQ + row;
+      uint16_t* dst = out + (static_cast<size_t>(b) * T + tq_row) * out_stride + h * HD;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t o[32];
-        tmem_ld_32x32b_x32(tO + lane_off + half * 32, o);
+        tmem_ld_32x32b_x32(tO(t) + lane_off + half * 32, o);
         tmem_ld_wait();
-        if (t < T) {
+        if (tq_row < T) {
           uint4* d4 = reinterpret_cast<uint4*>(dst + half * 32);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -305,7 +358,7 @@ cudaError_t launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const
     configured_device = dev;
   }
   const float scale_log2 = 1.4426950408889634f / 8.0f;  // log2(e) / sqrt(64)
-  dim3 grid((T + BQ - 1) / BQ, H, B);
+  dim3 grid((T + 2 * BQ - 1) / (2 * BQ), H, B);
   attn_fwd_kernel<<<grid, kThreads, SMEM, stream>>>(tq, tk, tv, q_col0, k_col0, v_col0, out, out_stride, T, scale_log2,
                                                      err);
   return cudaGetLastError();

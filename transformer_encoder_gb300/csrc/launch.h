@@ -36,11 +36,12 @@ cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmW, int M, i
                         cudaStream_t stream);
 
 // ---------------------------------------------------------------- attention (tcgen05)
-// Q/K/V tiles are read through 3-D maps [B][T][row] (box 64 x 128 for Q, 64 x 64 for K, V);
-// head h of Q, K, V starts at column q_col0 + 64h, k_col0 + 64h, v_col0 + 64h.
+// Q/K/V tiles are read through 3-D maps [B][T][row] (box 64 x 128 elements for all three);
+// head h of Q, K, V starts at column q_col0 + 64h, k_col0 + 64h, v_col0 + 64h. One CTA covers
+// 2 * kAttnBQ query rows of one (window, head).
 // out: bf16, row (b*T + t) at out + (b*T+t)*out_stride + 64h.
 constexpr int kAttnBQ = 128;
-constexpr int kAttnBKV = 64;
+constexpr int kAttnBKV = 128;
 cudaError_t launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, int q_col0,
                              int k_col0, int v_col0, uint16_t* out, int out_stride, int B, int T, int H,
                              uint32_t* err, cudaStream_t stream);
