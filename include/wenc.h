@@ -167,6 +167,14 @@ WENC_API wenc_status wenc_linear(const uint16_t* A, const uint16_t* W, const flo
                         const float* resid, void* out, int M, int N, int K, int epilogue,
                         wenc_stream_t stream);
 
+/* wenc_selftest_wait_timeout -- exercises the failure path of the bounded device waits
+ * (section "Failure detection" of the design; the pages have no counterpart). Launches one CTA
+ * that waits on an mbarrier nothing ever arrives on, with the same bounded wait every kernel
+ * uses: after about one second the wait gives up, records WENC_ERR_DEVICE_TIMEOUT (site 99)
+ * in the handle-less device error word and the kernel returns; no trap, the context stays
+ * usable. Stream-ordered; read the outcome with wenc_sync_status(NULL). */
+WENC_API wenc_status wenc_selftest_wait_timeout(wenc_stream_t stream);
+
 /* wenc_sync_status -- synchronise the device and read the device error word of `h`
  * (or, when h is NULL, the word shared by the handle-less entry points), clearing it.
  * Returns WENC_OK, WENC_ERR_DEVICE_TIMEOUT or WENC_ERR_CUDA. */

@@ -45,7 +45,7 @@ def test_layernorm_matches_oracle(rows, d, out_bf16):
 
 # ----------------------------------------------------------------------------- GEMM + epilogues
 @pytest.mark.parametrize("M,N,K", [(1537, 1152, 384), (300, 384, 1536), (1500, 2048, 512), (129, 256, 64),
-                                   (3000, 1280, 1280)])
+                                   (3000, 1280, 1280), (6000, 1280, 512), (1537, 640, 256)])
 @pytest.mark.parametrize("epi", [0, 1, 2])
 def test_linear_matches_oracle(M, N, K, epi):
     torch = _torch()

@@ -5,6 +5,6 @@ a fused flash-attention kernel, a warp-per-row LayerNorm); ``wenc`` is its ctype
 binding. PyTorch is used only for device memory and streams.
 """
 from .wenc import (  # noqa: F401
-    WencError, Encoder, attention, layernorm, linear, sync_status, lib, lib_path,
+    WencError, Encoder, attention, layernorm, linear, sync_status, selftest_wait_timeout, lib, lib_path,
     EPI_BIAS_BF16, EPI_BIAS_GELU_BF16, EPI_BIAS_RESID_F32, EXPORTED_SYMBOLS, LAUNCH_KINDS,
 )

@@ -19,6 +19,7 @@
 #include <vector>
 
 #include "launch.h"
+#include "ptx.cuh"
 #include "wenc.h"
 
 namespace {
@@ -113,6 +114,21 @@ int sm_count() {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
   return n > 0 ? n : 1;
+}
+
+// One CTA waits on a barrier that nothing arrives on; the bounded wait gives up, records the
+// timeout in the error word and the kernel returns normally.
+__global__ void stall_kernel(uint32_t* err) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  if (threadIdx.x == 0) {
+    wenc_dev::mbar_init(wenc_dev::smem_u32(&bar), 1);
+    abort_flag = 0u;
+    wenc_dev::fence_barrier_init();
+  }
+  __syncthreads();
+  const wenc_dev::WaitCtx wc{&abort_flag, err};
+  wenc_dev::mbar_wait(wenc_dev::smem_u32(&bar), 0, wc, 99);
 }
 
 }  // namespace
@@ -564,6 +580,17 @@ wenc_status wenc_linear(const uint16_t* A, const uint16_t* W, const float* bias,
   cudaError_t e = wenc_host::launch_gemm(ta, tw, M, N, K, bn, epilogue, bias, resid, out, err, sm_count(),
                                          reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "linear launch");
+  return WENC_OK;
+}
+
+wenc_status wenc_selftest_wait_timeout(wenc_stream_t stream) {
+  g_last_error.clear();
+  std::string why;
+  uint32_t* err = global_error_word(&why);
+  if (!err) return fail(WENC_ERR_CUDA, "%s", why.c_str());
+  stall_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
   return WENC_OK;
 }
 

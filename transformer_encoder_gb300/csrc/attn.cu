@@ -121,6 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_trigger();  // TMEM is held: the next kernel may be scheduled
+  pdl_wait();     // Q, K, V from the previous kernel are complete from here on
   auto tS = [&](int t) { return tmem_base + 128u * t; };
   auto tO = [&](int t) { return tmem_base + 256u + 64u * t; };
 
@@ -359,9 +361,8 @@ cudaError_t launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const
   }
   const float scale_log2 = 1.4426950408889634f / 8.0f;  // log2(e) / sqrt(64)
   dim3 grid((T + 2 * BQ - 1) / (2 * BQ), H, B);
-  attn_fwd_kernel<<<grid, kThreads, SMEM, stream>>>(tq, tk, tv, q_col0, k_col0, v_col0, out, out_stride, T, scale_log2,
-                                                     err);
-  return cudaGetLastError();
+  return launch_pdl(attn_fwd_kernel, grid, dim3(kThreads), SMEM, stream, tq, tk, tv, q_col0, k_col0, v_col0, out,
+                    out_stride, T, scale_log2, err);
 }
 
 }  // namespace wenc_host

@@ -171,6 +171,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_trigger();  // TMEM is held: the next kernel may be scheduled
+  pdl_wait();     // the previous kernel's outputs (A, residual) are complete from here on
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer
@@ -306,8 +308,8 @@ cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmW, int M, in
   }
   const int tiles = ((M + BM - 1) / BM) * (N / BN);
   const int grid = tiles < num_sms ? tiles : num_sms;
-  kern<<<grid, kThreads, C::SMEM, stream>>>(tmA, tmW, M, N, K, bias, resid, out, err);
-  return cudaGetLastError();
+  return wenc_host::launch_pdl(kern, dim3(grid), dim3(kThreads), C::SMEM, stream, tmA, tmW, M, N, K, bias, resid, out,
+                               err);
 }
 
 }  // namespace

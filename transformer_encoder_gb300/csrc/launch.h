@@ -6,8 +6,27 @@
 #include <stdint.h>
 
 #include <string>
+#include <utility>
 
 namespace wenc_host {
+
+// Launch with programmatic stream serialisation (the kernel overlaps its set-up with the tail of
+// the previous kernel in the stream; see pdl_wait / pdl_trigger in ptx.cuh).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Tensor-map construction (cuTensorMapEncodeTiled through the runtime's driver entry
 // point, so the library does not link libcuda directly).

@@ -30,6 +30,8 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock)
     layernorm_kernel(const float* __restrict__ x, const float* __restrict__ w, const float* __restrict__ b,
                      void* __restrict__ y, int rows, float eps) {
   constexpr int D = NV * 128;
+  wenc_dev::pdl_trigger();
+  wenc_dev::pdl_wait();  // x from the previous kernel is complete from here on
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
   if (row >= rows) return;
@@ -74,10 +76,10 @@ cudaError_t launch_nv(const float* x, const float* w, const float* b, void* y, i
                       cudaStream_t stream) {
   const int grid = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
   if (out_bf16)
-    layernorm_kernel<NV, true><<<grid, 32 * kRowsPerBlock, 0, stream>>>(x, w, b, y, rows, eps);
-  else
-    layernorm_kernel<NV, false><<<grid, 32 * kRowsPerBlock, 0, stream>>>(x, w, b, y, rows, eps);
-  return cudaGetLastError();
+    return wenc_host::launch_pdl(layernorm_kernel<NV, true>, dim3(grid), dim3(32 * kRowsPerBlock), 0, stream, x, w, b,
+                                 y, rows, eps);
+  return wenc_host::launch_pdl(layernorm_kernel<NV, false>, dim3(grid), dim3(32 * kRowsPerBlock), 0, stream, x, w, b, y,
+                               rows, eps);
 }
 
 __global__ void f32_to_bf16_kernel(const float* __restrict__ src, uint16_t* __restrict__ dst, size_t n) {

@@ -221,6 +221,15 @@ __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// ------------------------------------------------------------------ programmatic dependent launch
+// A kernel launched with programmatic stream serialisation may start while the previous kernel
+// of the stream is still running. It must call pdl_wait() before its first global-memory access
+// (the wait returns once the previous grid has completed and its writes are visible), and calls
+// pdl_trigger() once every resource it allocates at start-up is held, so that the next kernel's
+// CTAs can be scheduled and run their own set-up meanwhile.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------ math helpers
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;

@@ -26,7 +26,7 @@ LAUNCH_KINDS = {0: "layernorm", 1: "gemm_qkv", 2: "attention", 3: "gemm_out", 4:
 EXPORTED_SYMBOLS = (
     "wenc_create", "wenc_forward", "wenc_forward_layers", "wenc_forward_launches", "wenc_set_launch_events",
     "wenc_attention", "wenc_layernorm", "wenc_linear", "wenc_sync_status", "wenc_destroy", "wenc_last_error",
-    "wenc_version",
+    "wenc_version", "wenc_selftest_wait_timeout",
 )
 
 
@@ -70,12 +70,14 @@ def lib() -> ctypes.CDLL:
         L.wenc_layernorm.argtypes = [vp, vp, vp, vp, i, i, f, i, vp]
         L.wenc_linear.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, vp]
         L.wenc_sync_status.argtypes = [vp]
+        L.wenc_selftest_wait_timeout.argtypes = [vp]
         L.wenc_destroy.argtypes = [vp]
         L.wenc_destroy.restype = None
         L.wenc_last_error.restype = ctypes.c_char_p
         L.wenc_version.restype = ctypes.c_char_p
         for name in ("wenc_create", "wenc_forward", "wenc_forward_layers", "wenc_set_launch_events", "wenc_attention",
-                     "wenc_layernorm", "wenc_linear", "wenc_sync_status", "wenc_forward_launches"):
+                     "wenc_layernorm", "wenc_linear", "wenc_sync_status", "wenc_forward_launches",
+                     "wenc_selftest_wait_timeout"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -232,6 +234,11 @@ def linear(a, w, bias, epilogue: int = EPI_BIAS_BF16, resid=None, out=None, stre
         out = torch.empty((M, N), dtype=dt, device=a.device)
     _check(lib().wenc_linear(_ptr(a), _ptr(w), _ptr(bias), _ptr(resid), _ptr(out), M, N, K, epilogue, _stream(stream)))
     return out
+
+
+def selftest_wait_timeout(stream=None):
+    """Launch the bounded-wait self-test (returns immediately; read it with sync_status())."""
+    _check(lib().wenc_selftest_wait_timeout(_stream(stream)))
 
 
 def sync_status(encoder: Encoder | None = None):
