@@ -138,7 +138,7 @@ WENC_API int wenc_forward_launches(const wenc* h, int first, int count, int appl
  * (each a cudaEvent_t created by the caller), for n_events >= launches + 1; the hook
  * then clears itself. kinds (may be NULL) receives, per launch, 0 = LayerNorm,
  * 1 = QKV GEMM, 2 = attention, 3 = out-proj GEMM, 4 = fc1 GEMM, 5 = fc2 GEMM,
- * 6 = final LayerNorm, 7 = copy. */
+ * 6 = final LayerNorm, 7 = copy, 8 = attention split-key merge (small batches only). */
 WENC_API wenc_status wenc_set_launch_events(wenc* h, void* const* events, int n_events, int* kinds);
 
 /* wenc_attention -- out = softmax(q k^T * hd^-0.5) v per (window, head), non-causal,

@@ -161,3 +161,25 @@ def test_argument_errors():
         q = torch.zeros(1, 8, 2, 32, dtype=torch.bfloat16, device="cuda")
         attention(q, q, q)
     enc.sync_status()
+
+
+def test_split_key_attention_edge_shape():
+    """T = 700 (six key tiles, the last with 60 keys), d = 128, one window: the handle splits the
+    keys one tile per CTA and merges the partial results; the block must still match the oracle."""
+    import torch
+    from dataclasses import replace
+    w = replace(synth.WORKLOADS["tiny_block"], name="split_edge", d_model=128, n_heads=2, ffn_dim=256, seq_len=700)
+    enc, layers, _, rng = make_encoder(w)
+    assert enc.launches() == 8  # seven block launches plus the split-key merge
+    x = synth.make_input(w, rng)
+    y = enc.forward(_t(x))
+    torch.cuda.synchronize()
+    enc.sync_status()
+    y_ref = oracle.encoder_block(x, layers[0], w.n_heads)
+    _block_gates(x.astype(np.float64), y.cpu().numpy(), y_ref, "split-key block")
+
+
+def test_tiny_block_uses_split_keys():
+    w = synth.WORKLOADS["tiny_block"]
+    enc, _, _, _ = make_encoder(w)
+    assert enc.launches() == 8  # 36 query-pair CTAs would fill a quarter of the GPU: keys are split

@@ -203,6 +203,9 @@ struct wenc {
   float* x = nullptr;
   uint16_t *xn = nullptr, *qkv = nullptr, *o = nullptr, *u = nullptr;
   CUtensorMap tm_xn, tm_o, tm_u, tm_q, tm_kv;
+  int attn_splits = 1;            // key splits of the attention (1 = none), fixed at create
+  float* part_o = nullptr;        // split-key partial numerators (workspace)
+  float2* part_ml = nullptr;      // split-key (max, sum) pairs (workspace)
   void* weight_arena = nullptr;
   void* work_arena = nullptr;
   uint32_t* err_host = nullptr;  // mapped pinned word: the device writes, the host reads without a sync
@@ -330,6 +333,11 @@ wenc_status wenc_create(const wenc_config* cfg, const wenc_layer_weights* layers
   Arena ka;
   const size_t off_x = ka.take(rows * d * 4), off_xn = ka.take(rows * d * 2), off_qkv = ka.take(rows * 3 * d * 2),
                off_o = ka.take(rows * d * 2), off_u = ka.take(rows * f * 2);
+  // Small batches leave most SMs idle in attention: split the keys among more CTAs then.
+  h->attn_splits = wenc_host::attention_pick_splits(cfg->max_batch, cfg->seq_len, cfg->n_heads, h->num_sms);
+  const size_t part_rows = static_cast<size_t>(h->attn_splits) * cfg->max_batch * cfg->n_heads * cfg->seq_len;
+  const size_t off_po = h->attn_splits > 1 ? ka.take(part_rows * wenc_host::kAttnHD * sizeof(float)) : 0;
+  const size_t off_pml = h->attn_splits > 1 ? ka.take(part_rows * sizeof(float2)) : 0;
   e = cudaMalloc(&h->work_arena, ka.used);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -342,6 +350,10 @@ wenc_status wenc_create(const wenc_config* cfg, const wenc_layer_weights* layers
   h->qkv = reinterpret_cast<uint16_t*>(kb + off_qkv);
   h->o = reinterpret_cast<uint16_t*>(kb + off_o);
   h->u = reinterpret_cast<uint16_t*>(kb + off_u);
+  if (h->attn_splits > 1) {
+    h->part_o = reinterpret_cast<float*>(kb + off_po);
+    h->part_ml = reinterpret_cast<float2*>(kb + off_pml);
+  }
 
   e = cudaHostAlloc(reinterpret_cast<void**>(&h->err_host), sizeof(uint32_t), cudaHostAllocMapped);
   if (e != cudaSuccess) {
@@ -428,7 +440,7 @@ wenc_status wenc_create(const wenc_config* cfg, const wenc_layer_weights* layers
 int wenc_forward_launches(const wenc* h, int first, int count, int apply_final_ln) {
   if (!h || first < 0 || count < 0 || first + count > h->cfg.n_layers) return -1;
   const bool final_ln = apply_final_ln && h->cfg.final_ln;
-  int n = 7 * count;
+  int n = (6 + wenc_host::attention_launches(h->cfg.seq_len, h->attn_splits)) * count;
   if (final_ln) n += 1;
   else if (count == 0) n += 1;  // the copy in -> out
   return n;
@@ -492,7 +504,10 @@ wenc_status wenc_forward_layers(wenc* h, const float* in, float* out, int B, int
     rec(0, wenc_host::launch_layernorm(src, P.ln1_w, P.ln1_b, h->xn, M, d, c.ln_eps, true, s));
     rec(1, wenc_host::launch_gemm(h->tm_xn, P.tm_wqkv, M, 3 * d, d, h->bn_qkv, WENC_EPI_BIAS_BF16, P.bqkv, nullptr,
                                   h->qkv, h->err_dev, h->num_sms, s));
-    rec(2, wenc_host::launch_attention(h->tm_q, h->tm_kv, h->tm_kv, 0, d, 2 * d, h->o, d, B, T, H, h->err_dev, s));
+    rec(2, wenc_host::launch_attention_main(h->tm_q, h->tm_kv, h->tm_kv, 0, d, 2 * d, h->o, d, B, T, H, h->err_dev, s,
+                                            h->attn_splits, h->part_o, h->part_ml));
+    if (wenc_host::attention_launches(T, h->attn_splits) == 2)
+      rec(8, wenc_host::launch_attention_combine(h->part_o, h->part_ml, h->o, d, B, T, H, h->attn_splits, s));
     rec(3, wenc_host::launch_gemm(h->tm_o, P.tm_wo, M, d, d, h->bn_o, WENC_EPI_BIAS_RESID_F32, P.bo, src, h->x,
                                   h->err_dev, h->num_sms, s));
     rec(0, wenc_host::launch_layernorm(h->x, P.ln2_w, P.ln2_b, h->xn, M, d, c.ln_eps, true, s));

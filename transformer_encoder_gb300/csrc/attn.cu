@@ -60,7 +60,8 @@ constexpr float kRescaleThreshold = 8.0f;
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, int q_col0, int k_col0, int v_col0,
-                    uint16_t* __restrict__ out, int out_stride, int T, float scale_log2, uint32_t* err) {
+                    uint16_t* __restrict__ out, int out_stride, int T, float scale_log2, int n_splits,
+                    int tiles_per_split, float* __restrict__ part_o, float2* __restrict__ part_ml, uint32_t* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s0 = smem_u32(smem);
@@ -84,10 +85,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int q0 = blockIdx.x * 2 * BQ;
+  // blockIdx.x = query-pair index * n_splits + split; a split covers key tiles
+  // [kv0, kv0 + n_kv) of the window (all of them when n_splits == 1).
+  const int split = blockIdx.x % n_splits;
+  const int q0 = (blockIdx.x / n_splits) * 2 * BQ;
   const int h = blockIdx.y;
   const int b = blockIdx.z;
-  const int n_kv = (T + BKV - 1) / BKV;
+  const int kv0 = split * tiles_per_split;
+  const int n_kv = min(tiles_per_split, (T + BKV - 1) / BKV - kv0);  // >= 1 by construction
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -136,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int st = j % NK;
       if (!mbar_wait(k_empty(st), ((j / NK) & 1) ^ 1u, wc, 11)) return false;
       mbar_arrive_expect_tx(k_full(st), KV_BYTES);
-      tma_load_3d(sK + st * KV_BYTES, &tk, k_full(st), k_col0 + h * HD, j * BKV, b);
+      tma_load_3d(sK + st * KV_BYTES, &tk, k_full(st), k_col0 + h * HD, (kv0 + j) * BKV, b);
       k_issued = j + 1;
       return true;
     };
@@ -144,7 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int st = j % NV;
       if (!mbar_wait(v_empty(st), ((j / NV) & 1) ^ 1u, wc, 10)) return false;
       mbar_arrive_expect_tx(v_full(st), KV_BYTES);
-      tma_load_3d(sV + st * KV_BYTES, &tv, v_full(st), v_col0 + h * HD, j * BKV, b);
+      tma_load_3d(sV + st * KV_BYTES, &tv, v_full(st), v_col0 + h * HD, (kv0 + j) * BKV, b);
       v_issued = j + 1;
       return true;
     };
@@ -231,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(s_free(t));  // the MMA may overwrite S with the next tile
 
-      const int valid = T - j * BKV;  // keys of this tile inside the window
+      const int valid = T - (kv0 + j) * BKV;  // keys of this tile inside the window
       if (valid < BKV) {              // only a window's last tile can be partial (warp-uniform)
 #pragma unroll
         for (int c = 0; c < 128; ++c) sv[c] = (c < valid) ? sv[c] : -CUDART_INF_F;
@@ -314,23 +319,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ok && mbar_wait_warp(pv_done(t), (n_kv - 1) & 1, wc, 19)) {
       tc_fence_after();
-      const float inv_l = 1.0f / l;
       const int tq_row = q0 + t * BQ + row;
-      uint16_t* dst = out + (static_cast<size_t>(b) * T + tq_row) * out_stride + h * HD;
+      if (n_splits == 1) {
+        const float inv_l = 1.0f / l;
+        uint16_t* dst = out + (static_cast<size_t>(b) * T + tq_row) * out_stride + h * HD;
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t o[32];
-        tmem_ld_32x32b_x32(tO(t) + lane_off + half * 32, o);
-        tmem_ld_wait();
-        if (tq_row < T) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + half * 32);
+        for (int half = 0; half < 2; ++half) {
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(tO(t) + lane_off + half * 32, o);
+          tmem_ld_wait();
+          if (tq_row < T) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + half * 32);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float* f = reinterpret_cast<const float*>(o) + q * 8;
-            d4[q] = make_uint4(pack_bf16x2(f[0] * inv_l, f[1] * inv_l), pack_bf16x2(f[2] * inv_l, f[3] * inv_l),
-                               pack_bf16x2(f[4] * inv_l, f[5] * inv_l), pack_bf16x2(f[6] * inv_l, f[7] * inv_l));
+            for (int q = 0; q < 4; ++q) {
+              const float* f = reinterpret_cast<const float*>(o) + q * 8;
+              d4[q] = make_uint4(pack_bf16x2(f[0] * inv_l, f[1] * inv_l), pack_bf16x2(f[2] * inv_l, f[3] * inv_l),
+                                 pack_bf16x2(f[4] * inv_l, f[5] * inv_l), pack_bf16x2(f[6] * inv_l, f[7] * inv_l));
+            }
           }
         }
+      } else {
+        // Split keys: keep this split's unnormalised numerator, its reference maximum m (log2
+        // units, scores pre-scaled) and its denominator l for the combine kernel.
+        const size_t pi = (static_cast<size_t>(b * gridDim.y + h) * n_splits + split) * T + tq_row;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(tO(t) + lane_off + half * 32, o);
+          tmem_ld_wait();
+          if (tq_row < T) {
+            float4* d4 = reinterpret_cast<float4*>(part_o + pi * HD + half * 32);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              d4[q] = make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]),
+                                  __uint_as_float(o[4 * q + 2]), __uint_as_float(o[4 * q + 3]));
+          }
+        }
+        if (tq_row < T) part_ml[pi] = make_float2(m, l);
       }
     }
   }
@@ -343,13 +368,74 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Merge of the key splits of one (window, head, query row): with per-split maximum m_s,
+// denominator l_s and numerator O_s, m = max_s m_s and
+//   o = sum_s 2^(m_s - m) O_s / sum_s 2^(m_s - m) l_s
+// (the chunked merge of oxinfer 0.0.5 src/whisper/model.rs, CrossLayer::attend: per-chunk
+// maximum, sum and partial product, combined with exp(m_c - m) weights). Sixteen lanes per
+// (row, head), four output columns each.
+__global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restrict__ part_o,
+                                                           const float2* __restrict__ part_ml,
+                                                           uint16_t* __restrict__ out, int out_stride, int B,
+                                                           int T, int H, int n_splits) {
+  pdl_trigger();
+  pdl_wait();
+  const long long pair = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 4;
+  const int c4 = threadIdx.x & 15;
+  if (pair >= static_cast<long long>(B) * H * T) return;
+  const int t = static_cast<int>(pair % T);
+  const int h = static_cast<int>((pair / T) % H);
+  const int b = static_cast<int>(pair / (static_cast<long long>(T) * H));
+  const size_t base = static_cast<size_t>(b * H + h) * n_splits;
+  float mmax = -CUDART_INF_F;
+  for (int sp = 0; sp < n_splits; ++sp) mmax = fmaxf(mmax, part_ml[(base + sp) * T + t].x);
+  float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+  float den = 0.f;
+  for (int sp = 0; sp < n_splits; ++sp) {
+    const size_t pi = (base + sp) * T + t;
+    const float2 ml = part_ml[pi];
+    const float wgt = ex2_approx(ml.x - mmax);
+    const float4 o = reinterpret_cast<const float4*>(part_o + pi * HD)[c4];
+    num.x += wgt * o.x; num.y += wgt * o.y; num.z += wgt * o.z; num.w += wgt * o.w;
+    den += wgt * ml.y;
+  }
+  const float inv = 1.0f / den;
+  uint16_t* dst = out + (static_cast<size_t>(b) * T + t) * out_stride + h * HD + 4 * c4;
+  *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(num.x * inv, num.y * inv), pack_bf16x2(num.z * inv, num.w * inv));
+}
+
 }  // namespace
 
 namespace wenc_host {
 
-cudaError_t launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, int q_col0,
-                             int k_col0, int v_col0, uint16_t* out, int out_stride, int B, int T, int H,
-                             uint32_t* err, cudaStream_t stream) {
+int attention_pick_splits(int B, int T, int H, int num_sms) {
+  const long long ctas = static_cast<long long>((T + 2 * kAttnBQ - 1) / (2 * kAttnBQ)) * H * B;
+  const int n_kv = (T + kAttnBKV - 1) / kAttnBKV;
+  if (2 * ctas > num_sms || n_kv < 2) return 1;
+  int s = static_cast<int>(num_sms / ctas);
+  if (s > n_kv) s = n_kv;
+  // equal tile counts per split, none empty
+  const int tps = (n_kv + s - 1) / s;
+  return (n_kv + tps - 1) / tps;
+}
+
+size_t attention_partial_bytes(int B, int T, int H, int n_splits) {
+  if (n_splits <= 1) return 0;
+  const size_t rows = static_cast<size_t>(n_splits) * B * H * T;
+  return rows * kAttnHD * sizeof(float) + rows * sizeof(float2);
+}
+
+static int clamp_splits(int T, int n_splits) {
+  const int n_kv = (T + BKV - 1) / BKV;
+  if (n_splits < 1) n_splits = 1;
+  if (n_splits > n_kv) n_splits = n_kv;
+  const int tps = (n_kv + n_splits - 1) / n_splits;
+  return (n_kv + tps - 1) / tps;  // no empty split
+}
+
+cudaError_t launch_attention_main(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, int q_col0,
+                                  int k_col0, int v_col0, uint16_t* out, int out_stride, int B, int T, int H,
+                                  uint32_t* err, cudaStream_t stream, int n_splits, float* part_o, float2* part_ml) {
   if (B <= 0 || T <= 0 || H <= 0) return cudaSuccess;
   static int configured_device = -1;
   int dev = 0;
@@ -360,9 +446,34 @@ cudaError_t launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const
     configured_device = dev;
   }
   const float scale_log2 = 1.4426950408889634f / 8.0f;  // log2(e) / sqrt(64)
-  dim3 grid((T + 2 * BQ - 1) / (2 * BQ), H, B);
+  if (!part_o || !part_ml) n_splits = 1;
+  n_splits = clamp_splits(T, n_splits);
+  const int n_kv = (T + BKV - 1) / BKV;
+  const int tps = (n_kv + n_splits - 1) / n_splits;
+  dim3 grid(((T + 2 * BQ - 1) / (2 * BQ)) * n_splits, H, B);
   return launch_pdl(attn_fwd_kernel, grid, dim3(kThreads), SMEM, stream, tq, tk, tv, q_col0, k_col0, v_col0, out,
-                    out_stride, T, scale_log2, err);
+                    out_stride, T, scale_log2, n_splits, tps, part_o, part_ml, err);
+}
+
+cudaError_t launch_attention_combine(const float* part_o, const float2* part_ml, uint16_t* out, int out_stride, int B,
+                                     int T, int H, int n_splits, cudaStream_t stream) {
+  n_splits = clamp_splits(T, n_splits);
+  if (n_splits == 1 || B <= 0 || T <= 0 || H <= 0) return cudaSuccess;
+  const long long threads = static_cast<long long>(B) * H * T * 16;
+  return launch_pdl(attn_combine_kernel, dim3(static_cast<unsigned>((threads + 255) / 256)), dim3(256), 0, stream,
+                    part_o, part_ml, out, out_stride, B, T, H, n_splits);
+}
+
+int attention_launches(int T, int n_splits) { return clamp_splits(T, n_splits) > 1 ? 2 : 1; }
+
+cudaError_t launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, int q_col0,
+                             int k_col0, int v_col0, uint16_t* out, int out_stride, int B, int T, int H,
+                             uint32_t* err, cudaStream_t stream, int n_splits, float* part_o, float2* part_ml) {
+  if (!part_o || !part_ml) n_splits = 1;
+  cudaError_t e = launch_attention_main(tq, tk, tv, q_col0, k_col0, v_col0, out, out_stride, B, T, H, err, stream,
+                                        n_splits, part_o, part_ml);
+  if (e != cudaSuccess) return e;
+  return launch_attention_combine(part_o, part_ml, out, out_stride, B, T, H, n_splits, stream);
 }
 
 }  // namespace wenc_host

@@ -59,11 +59,25 @@ cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmW, int M, i
 // head h of Q, K, V starts at column q_col0 + 64h, k_col0 + 64h, v_col0 + 64h. One CTA covers
 // 2 * kAttnBQ query rows of one (window, head).
 // out: bf16, row (b*T + t) at out + (b*T+t)*out_stride + 64h.
+// With n_splits > 1 the key tiles are divided among n_splits CTAs per query pair, which write
+// unnormalised partial results to part_o [n_splits*B*H*T, 64] and (max, sum) to part_ml; a second
+// kernel merges them into out. n_splits is clamped to the number of key tiles.
 constexpr int kAttnBQ = 128;
 constexpr int kAttnBKV = 128;
+constexpr int kAttnHD = 64;
+int attention_pick_splits(int B, int T, int H, int num_sms);  // 1 unless the grid would be small
+size_t attention_partial_bytes(int B, int T, int H, int n_splits);
 cudaError_t launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, int q_col0,
                              int k_col0, int v_col0, uint16_t* out, int out_stride, int B, int T, int H,
-                             uint32_t* err, cudaStream_t stream);
+                             uint32_t* err, cudaStream_t stream, int n_splits = 1, float* part_o = nullptr,
+                             float2* part_ml = nullptr);
+// The two launches of launch_attention, separately (for per-launch accounting).
+cudaError_t launch_attention_main(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, int q_col0,
+                                  int k_col0, int v_col0, uint16_t* out, int out_stride, int B, int T, int H,
+                                  uint32_t* err, cudaStream_t stream, int n_splits, float* part_o, float2* part_ml);
+cudaError_t launch_attention_combine(const float* part_o, const float2* part_ml, uint16_t* out, int out_stride, int B,
+                                     int T, int H, int n_splits, cudaStream_t stream);
+int attention_launches(int T, int n_splits);  // kernels one launch_attention makes (1 or 2)
 
 // ---------------------------------------------------------------- weight packing
 cudaError_t launch_f32_to_bf16(const float* src, uint16_t* dst, size_t n, cudaStream_t stream);
