@@ -152,6 +152,28 @@ WENC_API wenc_status wenc_set_launch_events(wenc* h, void* const* events, int n_
 WENC_API wenc_status wenc_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                            uint16_t* out, int B, int T, int H, int hd, wenc_stream_t stream);
 
+/* wenc_attention_static -- the attention of wenc_attention (same arguments, layouts, rounding
+ * and error reporting) for callers that must not allocate device memory: a host that only lends
+ * memory from its own fixed pool, a runtime that forbids allocation while it serves requests, or
+ * code that cannot afford the device synchronisation an allocation may cause. The pages have no
+ * counterpart to this entry point. The keys of each query pair are split among several CTAs and
+ * the partial results are merged by a second kernel; those partial results live in a static
+ * device buffer that belongs to the library image (wenc_attention_static_capacity() bytes,
+ * 16 MiB, held on every GPU that loads the library until the process exits) instead of memory
+ * allocated here. The call allocates nothing. Limits: it needs (splits * B * H * T) * 264 bytes
+ * of that buffer, at least two splits when T > 128; larger problems are rejected with
+ * WENC_ERR_INVALID_ARG and a message naming the sizes (wenc_attention handles any size).
+ * The first call on each device looks up the buffer's device address (cudaGetSymbolAddress
+ * with that device current); make that first call before any stream capture. Every call
+ * shares the one buffer: calls whose work overlaps on the GPU (other streams, other host
+ * threads) race and must be ordered by the caller. Nothing in the buffer needs clearing: each
+ * call writes every partial result it later reads. Stream-ordered; hd must be 64. */
+WENC_API wenc_status wenc_attention_static(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                           uint16_t* out, int B, int T, int H, int hd, wenc_stream_t stream);
+
+/* wenc_attention_static_capacity -- bytes of the static buffer wenc_attention_static uses. */
+WENC_API size_t wenc_attention_static_capacity(void);
+
 /* wenc_layernorm -- y = (x - mean) / sqrt(var + eps) * w + b per row of x float32
  * [rows, d] (biased variance; inferencelayer LN_SRC). y is bf16 when out_bf16 != 0 (the
  * cast that feeds the next GEMM), else float32. d a multiple of 128, <= 2048. Stream-ordered. */

@@ -263,6 +263,12 @@ cudaError_t pack_matrix(const void* src, int dtype, uint16_t* dst, size_t n, cud
 
 }  // namespace
 
+// Helpers shared with the other entry-point files (status message, error word, device checks).
+wenc_status wenc_internal_fail(wenc_status s, const char* msg) { return fail(s, "%s", msg); }
+uint32_t* wenc_internal_error_word(std::string* why) { return global_error_word(why); }
+bool wenc_internal_is_sm103(std::string* why) { return device_is_sm103(why); }
+int wenc_internal_sm_count() { return sm_count(); }
+
 extern "C" {
 
 const char* wenc_last_error(void) { return g_last_error.c_str(); }

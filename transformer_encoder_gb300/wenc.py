@@ -26,7 +26,7 @@ LAUNCH_KINDS = {0: "layernorm", 1: "gemm_qkv", 2: "attention", 3: "gemm_out", 4:
 EXPORTED_SYMBOLS = (
     "wenc_create", "wenc_forward", "wenc_forward_layers", "wenc_forward_launches", "wenc_set_launch_events",
     "wenc_attention", "wenc_layernorm", "wenc_linear", "wenc_sync_status", "wenc_destroy", "wenc_last_error",
-    "wenc_version", "wenc_selftest_wait_timeout",
+    "wenc_version", "wenc_selftest_wait_timeout", "wenc_attention_static", "wenc_attention_static_capacity",
 )
 
 
@@ -71,6 +71,10 @@ def lib() -> ctypes.CDLL:
         L.wenc_linear.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, vp]
         L.wenc_sync_status.argtypes = [vp]
         L.wenc_selftest_wait_timeout.argtypes = [vp]
+        L.wenc_attention_static.argtypes = [vp, vp, vp, vp, i, i, i, i, vp]
+        L.wenc_attention_static.restype = ctypes.c_int
+        L.wenc_attention_static_capacity.argtypes = []
+        L.wenc_attention_static_capacity.restype = ctypes.c_size_t
         L.wenc_destroy.argtypes = [vp]
         L.wenc_destroy.restype = None
         L.wenc_last_error.restype = ctypes.c_char_p
