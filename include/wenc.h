@@ -59,9 +59,18 @@ typedef enum {
  * oxinfer src/whisper/model.rs, Precision). */
 typedef enum { WENC_DTYPE_F32 = 0, WENC_DTYPE_BF16 = 1 } wenc_dtype;
 
-/* Arithmetic of the contractions. BF16: bf16 operands on the tensor cores with fp32
- * accumulation; LayerNorm statistics, softmax, GELU and the residual stream are fp32. */
-typedef enum { WENC_PREC_BF16 = 0 } wenc_precision;
+/* Arithmetic of the contractions. In both, LayerNorm statistics, softmax, GELU, the
+ * accumulators and the residual stream are fp32.
+ * BF16: bf16 operands on the tensor cores (kind::f16); matrices rounded to bf16 at create
+ *   (nearest-even), activations between kernels (LN output, Q/K/V, P, attention output,
+ *   fc1 output) stored as bf16.
+ * TF32: TF32 operands on the tensor cores (kind::tf32: 10 explicit mantissa bits, fp32
+ *   exponent range); matrices kept as fp32 rounded to TF32 at create (nearest, ties away
+ *   from zero; bf16 matrices are widened exactly), activations between kernels stored as
+ *   fp32 rounded to TF32 by the kernel that writes them. Twice the operand bytes and half
+ *   the tensor-core rate of BF16, for about sixteen times smaller operand rounding
+ *   (oxinfer src/whisper/model.rs, Precision: F32 beside Bf16). */
+typedef enum { WENC_PREC_BF16 = 0, WENC_PREC_TF32 = 1 } wenc_precision;
 
 /* Epilogues of wenc_linear (the fused forms the block uses). */
 typedef enum {
@@ -81,7 +90,7 @@ typedef struct {
   int final_ln;      /* nonzero: apply the final LayerNorm after the last block */
   float ln_eps;      /* LayerNorm epsilon (1e-5 on all three pages) */
   int weight_dtype;  /* wenc_dtype of the matrices in wenc_layer_weights */
-  int precision;     /* wenc_precision; only WENC_PREC_BF16 */
+  int precision;     /* wenc_precision: WENC_PREC_BF16 or WENC_PREC_TF32 */
 } wenc_config;
 
 /* One block's parameters, as DEVICE pointers owned by the caller. Matrices are
@@ -102,8 +111,8 @@ typedef struct {
 typedef struct wenc wenc; /* opaque handle */
 
 /* wenc_create -- validate `cfg`, pack the weights into library-owned device memory
- * (matrices rounded to bf16, nearest-even, as oxinfer make_lin does for Precision::Bf16;
- * Q/K/V packed into one [3d, d] matrix with a [3d] bias whose K slot is zero, the
+ * (matrices rounded to bf16, nearest-even, as oxinfer make_lin does for Precision::Bf16,
+ * or kept as fp32 rounded to TF32 when cfg->precision is WENC_PREC_TF32; Q/K/V packed into one [3d, d] matrix with a [3d] bias whose K slot is zero, the
  * layout of turbospark-runtime DecLayerGpu::self_qkv_w), and allocate the activation
  * workspace for cfg->max_batch windows (all scratch sized once, as turbospark-runtime's
  * engine does at open). `layers` holds cfg->n_layers entries; lnf_w/lnf_b [d] are read
@@ -175,10 +184,11 @@ WENC_API wenc_status wenc_attention_static(const uint16_t* q, const uint16_t* k,
 WENC_API size_t wenc_attention_static_capacity(void);
 
 /* wenc_layernorm -- y = (x - mean) / sqrt(var + eps) * w + b per row of x float32
- * [rows, d] (biased variance; inferencelayer LN_SRC). y is bf16 when out_bf16 != 0 (the
- * cast that feeds the next GEMM), else float32. d a multiple of 128, <= 2048. Stream-ordered. */
+ * [rows, d] (biased variance; inferencelayer LN_SRC). out_format: 0 = float32, 1 = bf16
+ * (the cast that feeds a BF16 GEMM), 2 = float32 rounded to TF32 (feeds a TF32 GEMM);
+ * anything else is INVALID_ARG. d a multiple of 128, <= 2048. Stream-ordered. */
 WENC_API wenc_status wenc_layernorm(const float* x, const float* w, const float* b, void* y, int rows,
-                           int d, float eps, int out_bf16, wenc_stream_t stream);
+                           int d, float eps, int out_format, wenc_stream_t stream);
 
 /* wenc_linear -- one contraction of the block with a fused epilogue (see wenc_epilogue):
  * A bf16 [M, K], W bf16 [N, K] (K-major, PyTorch layout), bias float32 [N], resid/out
@@ -189,8 +199,29 @@ WENC_API wenc_status wenc_linear(const uint16_t* A, const uint16_t* W, const flo
                         const float* resid, void* out, int M, int N, int K, int epilogue,
                         wenc_stream_t stream);
 
+/* wenc_linear_tf32 -- the contraction of wenc_linear in the TF32 precision: A float32
+ * [M, K], W float32 [N, K], both read by the tensor cores as TF32 (pass values already
+ * rounded to TF32 for round-to-nearest; other low mantissa bits are not used as such), fp32
+ * accumulation. Epilogues as wenc_epilogue, except that WENC_EPI_BIAS_BF16 and
+ * WENC_EPI_BIAS_GELU_BF16 write float32 rounded to TF32 instead of bf16; out is float32
+ * [M, N]. N a multiple of 128, K a multiple of 32, M >= 1; buffers 16-byte aligned.
+ * Stream-ordered; errors as wenc_linear. */
+WENC_API wenc_status wenc_linear_tf32(const float* A, const float* W, const float* bias,
+                                      const float* resid, float* out, int M, int N, int K, int epilogue,
+                                      wenc_stream_t stream);
+
+/* wenc_attention_tf32 -- the attention of wenc_attention in the TF32 precision: q, k, v, out
+ * float32 [B, T, H, hd] contiguous, caller-owned. Q K^T and P V run on the tensor cores with
+ * TF32 operands (q, k, v read as TF32: pass values already rounded to TF32), the
+ * probabilities are rounded to TF32 before the PV product, softmax and accumulation are fp32,
+ * and the output is float32 rounded to TF32. hd must be 64; 1 <= T <= 1<<20; B, H >= 1.
+ * Buffers 16-byte aligned. Stream-ordered; a stalled device wait is recorded as for
+ * wenc_attention. */
+WENC_API wenc_status wenc_attention_tf32(const float* q, const float* k, const float* v, float* out,
+                                         int B, int T, int H, int hd, wenc_stream_t stream);
+
 /* wenc_selftest_wait_timeout -- exercises the failure path of the bounded device waits
- * (section "Failure detection" of the design; the pages have no counterpart). Launches one CTA
+ * (the pages have no counterpart). Launches one CTA
  * that waits on an mbarrier nothing ever arrives on, with the same bounded wait every kernel
  * uses: after about one second the wait gives up, records WENC_ERR_DEVICE_TIMEOUT (site 99)
  * in the handle-less device error word and the kernel returns; no trap, the context stays

@@ -30,7 +30,7 @@ import numpy as np
 
 __all__ = [
     "Workload", "WORKLOADS", "LAYER_KEYS", "MATRIX_KEYS",
-    "f32_to_bf16_bits", "bf16_bits_to_f32", "round_to_bf16",
+    "f32_to_bf16_bits", "bf16_bits_to_f32", "round_to_bf16", "round_to_tf32",
     "make_layer", "make_weights", "make_input", "make_qkv",
 ]
 
@@ -92,6 +92,14 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
 def round_to_bf16(a: np.ndarray) -> np.ndarray:
     """float32 array whose values are exactly representable in bfloat16."""
     return bf16_bits_to_f32(f32_to_bf16_bits(a))
+
+
+def round_to_tf32(a: np.ndarray) -> np.ndarray:
+    """float32 array rounded to TF32 (10 explicit mantissa bits), nearest with ties away from
+    zero: the values a TF32 tensor-core operand holds exactly (finite inputs only)."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x1000) & 0xFFFFE000
+    return u.astype(np.uint32).view(np.float32)
 
 
 def _normal(rng: np.random.Generator, shape, std: float) -> np.ndarray:

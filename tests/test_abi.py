@@ -74,3 +74,23 @@ def test_host_side_argument_errors(L):
     assert L.wenc_linear(p, p, p, None, p, 10, 128, 64, 2, None) == 1  # residual epilogue without resid
     assert L.wenc_linear(p, p, p, None, p, 10, 100, 64, 0, None) == 2  # N not a multiple of 128
     L.wenc_destroy(None)
+
+
+def test_host_side_argument_errors_tf32(L):
+    from transformer_encoder_gb300.wenc import Config, PREC_TF32
+    out = ctypes.c_void_p(123)
+    cfg = Config(1, 384, 6, 64, 1536, 1500, 1, 0, 1e-5, 0, 7)  # unknown precision
+    assert L.wenc_create(ctypes.byref(cfg), None, None, None, None, ctypes.byref(out)) == 2
+    assert b"precision" in L.wenc_last_error()
+    cfg = Config(1, 384, 6, 64, 1536, 1500, 1, 0, 1e-5, 0, PREC_TF32)  # valid config, no layers
+    assert L.wenc_create(ctypes.byref(cfg), None, None, None, None, ctypes.byref(out)) == 1
+    assert b"layers" in L.wenc_last_error()
+    p = ctypes.c_void_p(256)
+    assert L.wenc_linear_tf32(p, p, p, None, p, 10, 128, 48, 0, None) == 2   # K not a multiple of 32
+    assert L.wenc_linear_tf32(p, p, p, None, p, 10, 128, 64, 2, None) == 1   # residual epilogue without resid
+    assert L.wenc_linear_tf32(p, p, p, None, p, 10, 128, 64, 3, None) == 1   # unknown epilogue
+    assert L.wenc_linear_tf32(p, p, p, None, p, 0, 128, 64, 0, None) == 1    # M < 1
+    assert L.wenc_attention_tf32(p, p, p, p, 1, 10, 2, 32, None) == 2       # hd != 64
+    assert L.wenc_attention_tf32(p, p, p, p, 1, 0, 2, 64, None) == 1        # T < 1
+    assert L.wenc_attention_tf32(p, p, None, p, 1, 10, 2, 64, None) == 1
+    assert L.wenc_layernorm(p, p, p, p, 10, 128, 1e-5, 3, None) == 1         # unknown output format

@@ -135,52 +135,55 @@ __global__ void stall_kernel(uint32_t* err) {
 
 namespace wenc_host {
 
-bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
-                       uint32_t box_inner, uint32_t box_outer, std::string* why) {
+// One 128-byte-swizzled tiled map of rank 2 or 3 (dims[0] innermost).
+static bool make_tmap(CUtensorMap* map, CUtensorMapDataType dt, uint32_t rank, const void* base, const cuuint64_t* dims,
+                      const cuuint64_t* strides, const cuuint32_t* box, std::string* why) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) {
     *why = "cuTensorMapEncodeTiled is not available from the driver";
     return false;
   }
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {row_stride_bytes};
-  cuuint32_t box[2] = {box_inner, box_outer};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, dt, rank, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     char b[160];
-    snprintf(b, sizeof(b), "cuTensorMapEncodeTiled(2d %llu x %llu) failed with %d", (unsigned long long)inner,
-             (unsigned long long)outer, static_cast<int>(r));
+    snprintf(b, sizeof(b), "cuTensorMapEncodeTiled(rank %u, %llu x %llu) failed with %d", rank,
+             (unsigned long long)dims[0], (unsigned long long)dims[1], static_cast<int>(r));
     *why = b;
     return false;
   }
   return true;
 }
 
+bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
+                       uint32_t box_inner, uint32_t box_outer, std::string* why) {
+  const cuuint64_t dims[2] = {inner, outer}, strides[1] = {row_stride_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  return make_tmap(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, why);
+}
+
+bool make_tmap_2d_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
+                      uint32_t box_inner, uint32_t box_outer, std::string* why) {
+  const cuuint64_t dims[2] = {inner, outer}, strides[1] = {row_stride_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  return make_tmap(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, why);
+}
+
 bool make_tmap_3d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t dim1, uint64_t dim2,
                        uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box_inner, uint32_t box1,
                        std::string* why) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) {
-    *why = "cuTensorMapEncodeTiled is not available from the driver";
-    return false;
-  }
-  cuuint64_t dims[3] = {inner, dim1, dim2};
-  cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
-  cuuint32_t box[3] = {box_inner, box1, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
-    char b[160];
-    snprintf(b, sizeof(b), "cuTensorMapEncodeTiled(3d) failed with %d", static_cast<int>(r));
-    *why = b;
-    return false;
-  }
-  return true;
+  const cuuint64_t dims[3] = {inner, dim1, dim2}, strides[2] = {stride1_bytes, stride2_bytes};
+  const cuuint32_t box[3] = {box_inner, box1, 1};
+  return make_tmap(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, why);
+}
+
+bool make_tmap_3d_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t dim1, uint64_t dim2,
+                      uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box_inner, uint32_t box1,
+                      std::string* why) {
+  const cuuint64_t dims[3] = {inner, dim1, dim2}, strides[2] = {stride1_bytes, stride2_bytes};
+  const cuuint32_t box[3] = {box_inner, box1, 1};
+  return make_tmap(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, why);
 }
 
 }  // namespace wenc_host
@@ -190,8 +193,10 @@ struct wenc {
   wenc_config cfg;
   int device = 0;
   int num_sms = 1;
+  bool tf32 = false;  // precision WENC_PREC_TF32: fp32 (TF32-rounded) matrices and activations
+  size_t esz = 2;     // bytes per matrix / GEMM-operand element: 2 (bf16) or 4 (fp32)
   struct Layer {
-    uint16_t *wqkv, *wo, *w1, *w2;  // bf16, [n_out, n_in]
+    void *wqkv, *wo, *w1, *w2;  // [n_out, n_in], bf16 or TF32-rounded fp32
     float *ln1_w, *ln1_b, *bqkv, *bo, *ln2_w, *ln2_b, *b1, *b2;
     CUtensorMap tm_wqkv, tm_wo, tm_w1, tm_w2;
   };
@@ -201,7 +206,7 @@ struct wenc {
   int bn_qkv = 0, bn_o = 0, bn_1 = 0, bn_2 = 0;
   // workspace (rows = max_batch * seq_len)
   float* x = nullptr;
-  uint16_t *xn = nullptr, *qkv = nullptr, *o = nullptr, *u = nullptr;
+  void *xn = nullptr, *qkv = nullptr, *o = nullptr, *u = nullptr;  // element size esz
   CUtensorMap tm_xn, tm_o, tm_u, tm_q, tm_kv;
   int attn_splits = 1;            // key splits of the attention (1 = none), fixed at create
   float* part_o = nullptr;        // split-key partial numerators (workspace)
@@ -243,7 +248,8 @@ wenc_status check_config(const wenc_config* c) {
   if (!(c->ln_eps >= 0.0f)) return fail(WENC_ERR_INVALID_ARG, "ln_eps must be >= 0");
   if (c->weight_dtype != WENC_DTYPE_F32 && c->weight_dtype != WENC_DTYPE_BF16)
     return fail(WENC_ERR_INVALID_ARG, "weight_dtype %d unknown", c->weight_dtype);
-  if (c->precision != WENC_PREC_BF16) return fail(WENC_ERR_UNSUPPORTED, "precision %d: only BF16", c->precision);
+  if (c->precision != WENC_PREC_BF16 && c->precision != WENC_PREC_TF32)
+    return fail(WENC_ERR_UNSUPPORTED, "precision %d unknown (BF16 = 0, TF32 = 1)", c->precision);
   return WENC_OK;
 }
 
@@ -255,10 +261,12 @@ void free_handle(wenc* h) {
   delete h;
 }
 
-// Copy (bf16 source) or round (f32 source) one matrix into the packed bf16 arena.
-cudaError_t pack_matrix(const void* src, int dtype, uint16_t* dst, size_t n, cudaStream_t s) {
+// One matrix into the packed arena. BF16 precision: copied (bf16 source) or rounded to bf16
+// (fp32 source). TF32 precision: widened (bf16 source, exact) or rounded to TF32 (fp32 source).
+cudaError_t pack_matrix(const void* src, int dtype, bool tf32, void* dst, size_t n, cudaStream_t s) {
+  if (tf32) return wenc_host::launch_to_tf32(src, dtype == WENC_DTYPE_BF16, static_cast<float*>(dst), n, s);
   if (dtype == WENC_DTYPE_BF16) return cudaMemcpyAsync(dst, src, n * 2, cudaMemcpyDeviceToDevice, s);
-  return wenc_host::launch_f32_to_bf16(static_cast<const float*>(src), dst, n, s);
+  return wenc_host::launch_f32_to_bf16(static_cast<const float*>(src), static_cast<uint16_t*>(dst), n, s);
 }
 
 }  // namespace
@@ -305,6 +313,9 @@ wenc_status wenc_create(const wenc_config* cfg, const wenc_layer_weights* layers
   h->cfg = *cfg;
   cudaGetDevice(&h->device);
   h->num_sms = sm_count();
+  h->tf32 = cfg->precision == WENC_PREC_TF32;
+  h->esz = h->tf32 ? 4 : 2;
+  const size_t es = h->esz;
   h->bn_qkv = wenc_host::gemm_pick_bn(3 * d);
   h->bn_o = wenc_host::gemm_pick_bn(d);
   h->bn_1 = wenc_host::gemm_pick_bn(f);
@@ -316,10 +327,10 @@ wenc_status wenc_create(const wenc_config* cfg, const wenc_layer_weights* layers
   std::vector<Off> offs(L);
   for (int l = 0; l < L; ++l) {
     Off& o = offs[l];
-    o.wqkv = wa.take(size_t(3) * d * d * 2);
-    o.wo = wa.take(size_t(d) * d * 2);
-    o.w1 = wa.take(size_t(f) * d * 2);
-    o.w2 = wa.take(size_t(d) * f * 2);
+    o.wqkv = wa.take(size_t(3) * d * d * es);
+    o.wo = wa.take(size_t(d) * d * es);
+    o.w1 = wa.take(size_t(f) * d * es);
+    o.w2 = wa.take(size_t(d) * f * es);
     o.ln1_w = wa.take(d * 4); o.ln1_b = wa.take(d * 4);
     o.bqkv = wa.take(3 * d * 4); o.bo = wa.take(d * 4);
     o.ln2_w = wa.take(d * 4); o.ln2_b = wa.take(d * 4);
@@ -337,10 +348,12 @@ wenc_status wenc_create(const wenc_config* cfg, const wenc_layer_weights* layers
   // ---- workspace arena
   const size_t rows = size_t(cfg->max_batch) * cfg->seq_len;
   Arena ka;
-  const size_t off_x = ka.take(rows * d * 4), off_xn = ka.take(rows * d * 2), off_qkv = ka.take(rows * 3 * d * 2),
-               off_o = ka.take(rows * d * 2), off_u = ka.take(rows * f * 2);
-  // Small batches leave most SMs idle in attention: split the keys among more CTAs then.
-  h->attn_splits = wenc_host::attention_pick_splits(cfg->max_batch, cfg->seq_len, cfg->n_heads, h->num_sms);
+  const size_t off_x = ka.take(rows * d * 4), off_xn = ka.take(rows * d * es), off_qkv = ka.take(rows * 3 * d * es),
+               off_o = ka.take(rows * d * es), off_u = ka.take(rows * f * es);
+  // Small batches leave most SMs idle in attention: split the keys among more CTAs then (the
+  // bf16 kernel only).
+  h->attn_splits =
+      h->tf32 ? 1 : wenc_host::attention_pick_splits(cfg->max_batch, cfg->seq_len, cfg->n_heads, h->num_sms);
   const size_t part_rows = static_cast<size_t>(h->attn_splits) * cfg->max_batch * cfg->n_heads * cfg->seq_len;
   const size_t off_po = h->attn_splits > 1 ? ka.take(part_rows * wenc_host::kAttnHD * sizeof(float)) : 0;
   const size_t off_pml = h->attn_splits > 1 ? ka.take(part_rows * sizeof(float2)) : 0;
@@ -352,10 +365,10 @@ wenc_status wenc_create(const wenc_config* cfg, const wenc_layer_weights* layers
   }
   uint8_t* kb = static_cast<uint8_t*>(h->work_arena);
   h->x = reinterpret_cast<float*>(kb + off_x);
-  h->xn = reinterpret_cast<uint16_t*>(kb + off_xn);
-  h->qkv = reinterpret_cast<uint16_t*>(kb + off_qkv);
-  h->o = reinterpret_cast<uint16_t*>(kb + off_o);
-  h->u = reinterpret_cast<uint16_t*>(kb + off_u);
+  h->xn = kb + off_xn;
+  h->qkv = kb + off_qkv;
+  h->o = kb + off_o;
+  h->u = kb + off_u;
   if (h->attn_splits > 1) {
     h->part_o = reinterpret_cast<float*>(kb + off_po);
     h->part_ml = reinterpret_cast<float2*>(kb + off_pml);
@@ -376,10 +389,10 @@ wenc_status wenc_create(const wenc_config* cfg, const wenc_layer_weights* layers
     const wenc_layer_weights& w = layers[l];
     const Off& o = offs[l];
     wenc::Layer& P = h->layers[l];
-    P.wqkv = reinterpret_cast<uint16_t*>(wb + o.wqkv);
-    P.wo = reinterpret_cast<uint16_t*>(wb + o.wo);
-    P.w1 = reinterpret_cast<uint16_t*>(wb + o.w1);
-    P.w2 = reinterpret_cast<uint16_t*>(wb + o.w2);
+    P.wqkv = wb + o.wqkv;
+    P.wo = wb + o.wo;
+    P.w1 = wb + o.w1;
+    P.w2 = wb + o.w2;
     P.ln1_w = reinterpret_cast<float*>(wb + o.ln1_w);
     P.ln1_b = reinterpret_cast<float*>(wb + o.ln1_b);
     P.bqkv = reinterpret_cast<float*>(wb + o.bqkv);
@@ -389,12 +402,14 @@ wenc_status wenc_create(const wenc_config* cfg, const wenc_layer_weights* layers
     P.b1 = reinterpret_cast<float*>(wb + o.b1);
     P.b2 = reinterpret_cast<float*>(wb + o.b2);
     const size_t dd = size_t(d) * d;
-    if (e == cudaSuccess) e = pack_matrix(w.wq, cfg->weight_dtype, P.wqkv, dd, s);
-    if (e == cudaSuccess) e = pack_matrix(w.wk, cfg->weight_dtype, P.wqkv + dd, dd, s);
-    if (e == cudaSuccess) e = pack_matrix(w.wv, cfg->weight_dtype, P.wqkv + 2 * dd, dd, s);
-    if (e == cudaSuccess) e = pack_matrix(w.wo, cfg->weight_dtype, P.wo, dd, s);
-    if (e == cudaSuccess) e = pack_matrix(w.w1, cfg->weight_dtype, P.w1, size_t(f) * d, s);
-    if (e == cudaSuccess) e = pack_matrix(w.w2, cfg->weight_dtype, P.w2, size_t(d) * f, s);
+    uint8_t* qkv_w = static_cast<uint8_t*>(P.wqkv);
+    const int wdt = cfg->weight_dtype;
+    if (e == cudaSuccess) e = pack_matrix(w.wq, wdt, h->tf32, qkv_w, dd, s);
+    if (e == cudaSuccess) e = pack_matrix(w.wk, wdt, h->tf32, qkv_w + dd * es, dd, s);
+    if (e == cudaSuccess) e = pack_matrix(w.wv, wdt, h->tf32, qkv_w + 2 * dd * es, dd, s);
+    if (e == cudaSuccess) e = pack_matrix(w.wo, wdt, h->tf32, P.wo, dd, s);
+    if (e == cudaSuccess) e = pack_matrix(w.w1, wdt, h->tf32, P.w1, size_t(f) * d, s);
+    if (e == cudaSuccess) e = pack_matrix(w.w2, wdt, h->tf32, P.w2, size_t(d) * f, s);
     auto cp = [&](float* dst, const float* src, size_t n) {
       if (e == cudaSuccess) e = cudaMemcpyAsync(dst, src, n * 4, cudaMemcpyDeviceToDevice, s);
     };
@@ -418,23 +433,36 @@ wenc_status wenc_create(const wenc_config* cfg, const wenc_layer_weights* layers
     return cuda_fail(e, "packing weights");
   }
 
-  // ---- tensor maps (all over library-owned buffers; built once)
+  // ---- tensor maps (all over library-owned buffers; built once). A stage row is 128 bytes:
+  // 64 bf16 or 32 fp32 elements.
   bool ok = true;
+  const uint32_t kbox = h->tf32 ? 32 : 64;
+  auto map2 = [&](CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+    ok = ok && (h->tf32 ? wenc_host::make_tmap_2d_f32(m, base, inner, outer, inner * 4, kbox, box_outer, &why)
+                        : wenc_host::make_tmap_2d_bf16(m, base, inner, outer, inner * 2, kbox, box_outer, &why));
+  };
   for (int l = 0; l < L && ok; ++l) {
     wenc::Layer& P = h->layers[l];
-    ok = ok && wenc_host::make_tmap_2d_bf16(&P.tm_wqkv, P.wqkv, d, 3 * d, size_t(d) * 2, 64, h->bn_qkv, &why);
-    ok = ok && wenc_host::make_tmap_2d_bf16(&P.tm_wo, P.wo, d, d, size_t(d) * 2, 64, h->bn_o, &why);
-    ok = ok && wenc_host::make_tmap_2d_bf16(&P.tm_w1, P.w1, d, f, size_t(d) * 2, 64, h->bn_1, &why);
-    ok = ok && wenc_host::make_tmap_2d_bf16(&P.tm_w2, P.w2, f, d, size_t(f) * 2, 64, h->bn_2, &why);
+    map2(&P.tm_wqkv, P.wqkv, d, 3 * d, h->bn_qkv);
+    map2(&P.tm_wo, P.wo, d, d, h->bn_o);
+    map2(&P.tm_w1, P.w1, d, f, h->bn_1);
+    map2(&P.tm_w2, P.w2, f, d, h->bn_2);
   }
-  ok = ok && wenc_host::make_tmap_2d_bf16(&h->tm_xn, h->xn, d, rows, size_t(d) * 2, 64, wenc_host::kGemmBM, &why);
-  ok = ok && wenc_host::make_tmap_2d_bf16(&h->tm_o, h->o, d, rows, size_t(d) * 2, 64, wenc_host::kGemmBM, &why);
-  ok = ok && wenc_host::make_tmap_2d_bf16(&h->tm_u, h->u, f, rows, size_t(f) * 2, 64, wenc_host::kGemmBM, &why);
-  const size_t qkv_row = size_t(3) * d * 2;
-  ok = ok && wenc_host::make_tmap_3d_bf16(&h->tm_q, h->qkv, 3 * d, cfg->seq_len, cfg->max_batch, qkv_row,
-                                          qkv_row * cfg->seq_len, 64, wenc_host::kAttnBQ, &why);
-  ok = ok && wenc_host::make_tmap_3d_bf16(&h->tm_kv, h->qkv, 3 * d, cfg->seq_len, cfg->max_batch, qkv_row,
-                                          qkv_row * cfg->seq_len, 64, wenc_host::kAttnBKV, &why);
+  map2(&h->tm_xn, h->xn, d, rows, wenc_host::kGemmBM);
+  map2(&h->tm_o, h->o, d, rows, wenc_host::kGemmBM);
+  map2(&h->tm_u, h->u, f, rows, wenc_host::kGemmBM);
+  const size_t qkv_row = size_t(3) * d * es;
+  if (h->tf32) {
+    ok = ok && wenc_host::make_tmap_3d_f32(&h->tm_q, h->qkv, 3 * d, cfg->seq_len, cfg->max_batch, qkv_row,
+                                           qkv_row * cfg->seq_len, 32, wenc_host::kAttnTf32BQ, &why);
+    ok = ok && wenc_host::make_tmap_3d_f32(&h->tm_kv, h->qkv, 3 * d, cfg->seq_len, cfg->max_batch, qkv_row,
+                                           qkv_row * cfg->seq_len, 32, wenc_host::kAttnTf32BKV, &why);
+  } else {
+    ok = ok && wenc_host::make_tmap_3d_bf16(&h->tm_q, h->qkv, 3 * d, cfg->seq_len, cfg->max_batch, qkv_row,
+                                            qkv_row * cfg->seq_len, 64, wenc_host::kAttnBQ, &why);
+    ok = ok && wenc_host::make_tmap_3d_bf16(&h->tm_kv, h->qkv, 3 * d, cfg->seq_len, cfg->max_batch, qkv_row,
+                                            qkv_row * cfg->seq_len, 64, wenc_host::kAttnBKV, &why);
+  }
   if (!ok) {
     free_handle(h);
     return fail(WENC_ERR_CUDA, "%s", why.c_str());
@@ -446,7 +474,8 @@ wenc_status wenc_create(const wenc_config* cfg, const wenc_layer_weights* layers
 int wenc_forward_launches(const wenc* h, int first, int count, int apply_final_ln) {
   if (!h || first < 0 || count < 0 || first + count > h->cfg.n_layers) return -1;
   const bool final_ln = apply_final_ln && h->cfg.final_ln;
-  int n = (6 + wenc_host::attention_launches(h->cfg.seq_len, h->attn_splits)) * count;
+  const int attn = h->tf32 ? 1 : wenc_host::attention_launches(h->cfg.seq_len, h->attn_splits);
+  int n = (6 + attn) * count;
   if (final_ln) n += 1;
   else if (count == 0) n += 1;  // the copy in -> out
   return n;
@@ -507,16 +536,34 @@ wenc_status wenc_forward_layers(wenc* h, const float* in, float* out, int B, int
     const wenc::Layer& P = h->layers[l];
     const bool last = (l == first + count - 1);
     float* dst_final = (last && !final_ln) ? out : h->x;
-    rec(0, wenc_host::launch_layernorm(src, P.ln1_w, P.ln1_b, h->xn, M, d, c.ln_eps, true, s));
+    if (h->tf32) {
+      // TF32: every GEMM operand is fp32 rounded to TF32 by its producer.
+      rec(0, wenc_host::launch_layernorm(src, P.ln1_w, P.ln1_b, h->xn, M, d, c.ln_eps, 2, s));
+      rec(1, wenc_host::launch_gemm(h->tm_xn, P.tm_wqkv, M, 3 * d, d, h->bn_qkv, WENC_EPI_BIAS_BF16, P.bqkv, nullptr,
+                                    h->qkv, h->err_dev, h->num_sms, s, true));
+      rec(2, wenc_host::launch_attention_tf32(h->tm_q, h->tm_kv, h->tm_kv, 0, d, 2 * d, static_cast<float*>(h->o), d,
+                                              B, T, H, h->err_dev, s));
+      rec(3, wenc_host::launch_gemm(h->tm_o, P.tm_wo, M, d, d, h->bn_o, WENC_EPI_BIAS_RESID_F32, P.bo, src, h->x,
+                                    h->err_dev, h->num_sms, s, true));
+      rec(0, wenc_host::launch_layernorm(h->x, P.ln2_w, P.ln2_b, h->xn, M, d, c.ln_eps, 2, s));
+      rec(4, wenc_host::launch_gemm(h->tm_xn, P.tm_w1, M, f, d, h->bn_1, WENC_EPI_BIAS_GELU_BF16, P.b1, nullptr, h->u,
+                                    h->err_dev, h->num_sms, s, true));
+      rec(5, wenc_host::launch_gemm(h->tm_u, P.tm_w2, M, d, f, h->bn_2, WENC_EPI_BIAS_RESID_F32, P.b2, h->x, dst_final,
+                                    h->err_dev, h->num_sms, s, true));
+      src = h->x;
+      continue;
+    }
+    uint16_t* o16 = static_cast<uint16_t*>(h->o);
+    rec(0, wenc_host::launch_layernorm(src, P.ln1_w, P.ln1_b, h->xn, M, d, c.ln_eps, 1, s));
     rec(1, wenc_host::launch_gemm(h->tm_xn, P.tm_wqkv, M, 3 * d, d, h->bn_qkv, WENC_EPI_BIAS_BF16, P.bqkv, nullptr,
                                   h->qkv, h->err_dev, h->num_sms, s));
-    rec(2, wenc_host::launch_attention_main(h->tm_q, h->tm_kv, h->tm_kv, 0, d, 2 * d, h->o, d, B, T, H, h->err_dev, s,
+    rec(2, wenc_host::launch_attention_main(h->tm_q, h->tm_kv, h->tm_kv, 0, d, 2 * d, o16, d, B, T, H, h->err_dev, s,
                                             h->attn_splits, h->part_o, h->part_ml));
     if (wenc_host::attention_launches(T, h->attn_splits) == 2)
-      rec(8, wenc_host::launch_attention_combine(h->part_o, h->part_ml, h->o, d, B, T, H, h->attn_splits, s));
+      rec(8, wenc_host::launch_attention_combine(h->part_o, h->part_ml, o16, d, B, T, H, h->attn_splits, s));
     rec(3, wenc_host::launch_gemm(h->tm_o, P.tm_wo, M, d, d, h->bn_o, WENC_EPI_BIAS_RESID_F32, P.bo, src, h->x,
                                   h->err_dev, h->num_sms, s));
-    rec(0, wenc_host::launch_layernorm(h->x, P.ln2_w, P.ln2_b, h->xn, M, d, c.ln_eps, true, s));
+    rec(0, wenc_host::launch_layernorm(h->x, P.ln2_w, P.ln2_b, h->xn, M, d, c.ln_eps, 1, s));
     rec(4, wenc_host::launch_gemm(h->tm_xn, P.tm_w1, M, f, d, h->bn_1, WENC_EPI_BIAS_GELU_BF16, P.b1, nullptr, h->u,
                                   h->err_dev, h->num_sms, s));
     rec(5, wenc_host::launch_gemm(h->tm_u, P.tm_w2, M, d, f, h->bn_2, WENC_EPI_BIAS_RESID_F32, P.b2, h->x, dst_final,
@@ -525,7 +572,7 @@ wenc_status wenc_forward_layers(wenc* h, const float* in, float* out, int B, int
   }
   if (e == cudaSuccess) {
     if (final_ln) {
-      rec(6, wenc_host::launch_layernorm(src, h->lnf_w, h->lnf_b, out, M, d, c.ln_eps, false, s));
+      rec(6, wenc_host::launch_layernorm(src, h->lnf_w, h->lnf_b, out, M, d, c.ln_eps, 0, s));
     } else if (count == 0) {
       rec(7, in == out ? cudaSuccess : cudaMemcpyAsync(out, in, size_t(M) * d * 4, cudaMemcpyDeviceToDevice, s));
     }
@@ -565,7 +612,7 @@ wenc_status wenc_attention(const uint16_t* q, const uint16_t* k, const uint16_t*
 }
 
 wenc_status wenc_layernorm(const float* x, const float* w, const float* b, void* y, int rows, int d, float eps,
-                           int out_bf16, wenc_stream_t stream) {
+                           int out_format, wenc_stream_t stream) {
   g_last_error.clear();
   if (!x || !w || !b || !y) return fail(WENC_ERR_INVALID_ARG, "x/w/b/y is NULL");
   if (rows < 1) return fail(WENC_ERR_INVALID_ARG, "rows must be >= 1");
@@ -573,7 +620,8 @@ wenc_status wenc_layernorm(const float* x, const float* w, const float* b, void*
   if (!(eps >= 0.0f)) return fail(WENC_ERR_INVALID_ARG, "eps must be >= 0");
   if (!aligned16(x) || !aligned16(w) || !aligned16(b) || !aligned16(y))
     return fail(WENC_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
-  cudaError_t e = wenc_host::launch_layernorm(x, w, b, y, rows, d, eps, out_bf16 != 0, reinterpret_cast<cudaStream_t>(stream));
+  if (out_format < 0 || out_format > 2) return fail(WENC_ERR_INVALID_ARG, "out_format %d unknown", out_format);
+  cudaError_t e = wenc_host::launch_layernorm(x, w, b, y, rows, d, eps, out_format, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "layernorm launch");
   return WENC_OK;
 }
@@ -601,6 +649,57 @@ wenc_status wenc_linear(const uint16_t* A, const uint16_t* W, const float* bias,
   cudaError_t e = wenc_host::launch_gemm(ta, tw, M, N, K, bn, epilogue, bias, resid, out, err, sm_count(),
                                          reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "linear launch");
+  return WENC_OK;
+}
+
+wenc_status wenc_linear_tf32(const float* A, const float* W, const float* bias, const float* resid, float* out, int M,
+                             int N, int K, int epilogue, wenc_stream_t stream) {
+  g_last_error.clear();
+  if (!A || !W || !bias || !out) return fail(WENC_ERR_INVALID_ARG, "A/W/bias/out is NULL");
+  if (epilogue < 0 || epilogue > 2) return fail(WENC_ERR_INVALID_ARG, "epilogue %d unknown", epilogue);
+  if (epilogue == WENC_EPI_BIAS_RESID_F32 && !resid) return fail(WENC_ERR_INVALID_ARG, "resid is NULL");
+  if (M < 1) return fail(WENC_ERR_INVALID_ARG, "M must be >= 1");
+  const int bn = wenc_host::gemm_pick_bn(N);
+  if (bn == 0) return fail(WENC_ERR_UNSUPPORTED, "N %d: must be a multiple of 128", N);
+  if (K < 32 || K % 32 != 0) return fail(WENC_ERR_UNSUPPORTED, "K %d: must be a positive multiple of 32", K);
+  if (!aligned16(A) || !aligned16(W) || !aligned16(bias) || !aligned16(out) || (resid && !aligned16(resid)))
+    return fail(WENC_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
+  std::string why;
+  if (!device_is_sm103(&why)) return fail(WENC_ERR_UNSUPPORTED, "%s", why.c_str());
+  uint32_t* err = global_error_word(&why);
+  if (!err) return fail(WENC_ERR_CUDA, "%s", why.c_str());
+  CUtensorMap ta, tw;
+  bool ok = wenc_host::make_tmap_2d_f32(&ta, A, K, M, size_t(K) * 4, 32, wenc_host::kGemmBM, &why) &&
+            wenc_host::make_tmap_2d_f32(&tw, W, K, N, size_t(K) * 4, 32, bn, &why);
+  if (!ok) return fail(WENC_ERR_INVALID_ARG, "%s", why.c_str());
+  cudaError_t e = wenc_host::launch_gemm(ta, tw, M, N, K, bn, epilogue, bias, resid, out, err, sm_count(),
+                                         reinterpret_cast<cudaStream_t>(stream), true);
+  if (e != cudaSuccess) return cuda_fail(e, "linear launch");
+  return WENC_OK;
+}
+
+wenc_status wenc_attention_tf32(const float* q, const float* k, const float* v, float* out, int B, int T, int H, int hd,
+                                wenc_stream_t stream) {
+  g_last_error.clear();
+  if (!q || !k || !v || !out) return fail(WENC_ERR_INVALID_ARG, "q/k/v/out is NULL");
+  if (B < 1 || T < 1 || H < 1) return fail(WENC_ERR_INVALID_ARG, "B, T, H must be >= 1");
+  if (hd != 64) return fail(WENC_ERR_UNSUPPORTED, "head_dim %d: only 64 is implemented", hd);
+  if (T > (1 << 20)) return fail(WENC_ERR_UNSUPPORTED, "T %d too large", T);
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(WENC_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
+  std::string why;
+  if (!device_is_sm103(&why)) return fail(WENC_ERR_UNSUPPORTED, "%s", why.c_str());
+  uint32_t* err = global_error_word(&why);
+  if (!err) return fail(WENC_ERR_CUDA, "%s", why.c_str());
+  const uint64_t row = uint64_t(H) * 64;
+  CUtensorMap tq, tk, tv;
+  bool ok = wenc_host::make_tmap_3d_f32(&tq, q, row, T, B, row * 4, row * 4 * T, 32, wenc_host::kAttnTf32BQ, &why) &&
+            wenc_host::make_tmap_3d_f32(&tk, k, row, T, B, row * 4, row * 4 * T, 32, wenc_host::kAttnTf32BKV, &why) &&
+            wenc_host::make_tmap_3d_f32(&tv, v, row, T, B, row * 4, row * 4 * T, 32, wenc_host::kAttnTf32BKV, &why);
+  if (!ok) return fail(WENC_ERR_INVALID_ARG, "%s", why.c_str());
+  cudaError_t e = wenc_host::launch_attention_tf32(tq, tk, tv, 0, 0, 0, out, static_cast<int>(row), B, T, H, err,
+                                                   reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   return WENC_OK;
 }
 

@@ -7,6 +7,8 @@
 //   QKV:      bf16 out = A W^T + b             (b's K slot is zero)
 //   fc1:      bf16 out = GELU_erf(A W^T + b)
 //   out, fc2: f32  out = resid + (A W^T + b)   (the residual add, in place on x)
+// The TF32 form of the kernel takes fp32 A and W (already rounded to TF32 by their producers)
+// and runs kind::tf32 MMAs (128 x BN x 8); its QKV and fc1 outputs are fp32 rounded to TF32.
 //
 // Design (sm_103a): persistent CTAs, one per SM, walk 128 x BN output tiles. Warp 0 is the
 // TMA producer (A and W tiles, 128-byte swizzle, a STAGES-deep mbarrier ring); warp 1
@@ -30,8 +32,9 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer warp, MMA warp, epilo
 template <int BN>
 struct GemmCfg {
   static constexpr int STAGES = (BN == 256) ? 4 : 6;
-  static constexpr uint32_t A_BYTES = BM * BK * 2;
-  static constexpr uint32_t B_BYTES = BN * BK * 2;
+  // One stage holds 128-byte rows: 64 bf16 or 32 fp32 elements of K.
+  static constexpr uint32_t A_BYTES = BM * 128;
+  static constexpr uint32_t B_BYTES = BN * 128;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TMEM_COLS = 2 * BN;  // two fp32 accumulators of BN columns
   static constexpr uint32_t NUM_BARS = 2 * STAGES + 5;
@@ -88,7 +91,9 @@ __device__ __forceinline__ void load_resid(float4 (&rr)[8], const float* resid, 
   }
 }
 
-template <int EPI>
+// EPI 0 = bias, 1 = bias + GELU, 2 = residual + bias (fp32 out). For EPI 0 and 1 the output
+// is bf16 (F32OUT false) or fp32 rounded to TF32 (F32OUT true: the operand of a TF32 GEMM).
+template <int EPI, bool F32OUT>
 __device__ __forceinline__ void epilogue_chunk(const uint32_t (&acc)[32], uint32_t stage, int lane, int grow0, int M,
                                                int N, int col, const float* __restrict__ bias,
                                                const float4 (&rr)[8], void* out) {
@@ -113,14 +118,19 @@ __device__ __forceinline__ void epilogue_chunk(const uint32_t (&acc)[32], uint32
         if constexpr (EPI == 1) {
           v.x = gelu_erf(v.x); v.y = gelu_erf(v.y); v.z = gelu_erf(v.z); v.w = gelu_erf(v.w);
         }
-        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + off) = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+        if constexpr (F32OUT)
+          *reinterpret_cast<float4*>(static_cast<float*>(out) + off) =
+              make_float4(round_tf32(v.x), round_tf32(v.y), round_tf32(v.z), round_tf32(v.w));
+        else
+          *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + off) =
+              make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
       }
     }
   }
   __syncwarp();  // the stage is rewritten by the next chunk
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool TF32>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, int M, int N,
                    int K, const float* __restrict__ bias, const float* resid, void* out, uint32_t* err) {
@@ -146,7 +156,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int m_tiles = (M + BM - 1) / BM;
   const int n_tiles = N / BN;
   const int num_tiles = m_tiles * n_tiles;
-  const int k_blocks = K / BK;
+  constexpr int BKE = TF32 ? 32 : BK;  // K elements per stage (128-byte rows)
+  const int k_blocks = K / BKE;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -186,8 +197,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kb = 0; kb < k_blocks; ++kb) {
         if (!mbar_wait(empty_bar(stage), phase ^ 1u, wc, 1)) { ok = false; break; }
         mbar_arrive_expect_tx(full_bar(stage), C::STAGE_BYTES);
-        tma_load_2d(sA + stage * C::A_BYTES, &tmA, full_bar(stage), kb * BK, m0);
-        tma_load_2d(sB + stage * C::B_BYTES, &tmW, full_bar(stage), kb * BK, n0);
+        tma_load_2d(sA + stage * C::A_BYTES, &tmA, full_bar(stage), kb * BKE, m0);
+        tma_load_2d(sB + stage * C::B_BYTES, &tmW, full_bar(stage), kb * BKE, n0);
         issued_mask |= 1u << stage;
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
@@ -202,7 +213,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------- UMMA issuer
-    constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, false);
+    // Four MMAs per stage, each over 32 bytes of K (16 bf16 or 8 TF32 elements).
+    constexpr uint32_t idesc = TF32 ? idesc_tf32_f32(BM, BN) : idesc_bf16_f32(BM, BN, false);
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
@@ -219,10 +231,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t a_base = sA + stage * C::A_BYTES;
         const uint32_t b_base = sB + stage * C::B_BYTES;
 #pragma unroll
-        for (int k = 0; k < BK / 16; ++k) {
+        for (int k = 0; k < 4; ++k) {
           const uint64_t ad = sdesc_sw128(a_base + k * 32, 16, 1024);
           const uint64_t bd = sdesc_sw128(b_base + k * 32, 16, 1024);
-          umma_bf16_ss(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+          if constexpr (TF32) umma_tf32_ss(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+          else umma_bf16_ss(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
         }
         umma_commit(empty_bar(stage));
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -273,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(tempty_bar(acc));
         }
-        epilogue_chunk<EPI>(r, stage, lane, grow0, M, N, c0 + c * 32, bias, rb[c & 1], out);
+        epilogue_chunk<EPI, TF32>(r, stage, lane, grow0, M, N, c0 + c * 32, bias, rb[c & 1], out);
         if constexpr (EPI == 2) {
           if (c + 2 < CH) {
             load_resid(rb[c & 1], resid, grow0, M, N, c0 + (c + 2) * 32, lane);
@@ -293,11 +306,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool TF32>
 cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmW, int M, int N, int K, const float* bias,
                        const float* resid, void* out, uint32_t* err, int num_sms, cudaStream_t stream) {
   using C = GemmCfg<BN>;
-  auto kern = gemm_tc_kernel<BN, EPI>;
+  auto kern = gemm_tc_kernel<BN, EPI, TF32>;
   static int configured_device = -1;  // attribute is per device; cheap to repeat
   int dev = 0;
   cudaGetDevice(&dev);
@@ -324,16 +337,23 @@ int gemm_pick_bn(int N) {
 
 cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmW, int M, int N, int K, int bn, int epilogue,
                         const float* bias, const float* resid, void* out, uint32_t* err, int num_sms,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, bool tf32) {
   if (M <= 0) return cudaSuccess;
-#define WENC_GEMM_CASE(BNV, EPIV) \
-  if (bn == BNV && epilogue == EPIV) return launch_one<BNV, EPIV>(tmA, tmW, M, N, K, bias, resid, out, err, num_sms, stream);
-  WENC_GEMM_CASE(256, 0)
-  WENC_GEMM_CASE(256, 1)
-  WENC_GEMM_CASE(256, 2)
-  WENC_GEMM_CASE(128, 0)
-  WENC_GEMM_CASE(128, 1)
-  WENC_GEMM_CASE(128, 2)
+#define WENC_GEMM_CASE(BNV, EPIV, TF) \
+  if (bn == BNV && epilogue == EPIV && tf32 == TF)                                        \
+    return launch_one<BNV, EPIV, TF>(tmA, tmW, M, N, K, bias, resid, out, err, num_sms, stream);
+  WENC_GEMM_CASE(256, 0, false)
+  WENC_GEMM_CASE(256, 1, false)
+  WENC_GEMM_CASE(256, 2, false)
+  WENC_GEMM_CASE(128, 0, false)
+  WENC_GEMM_CASE(128, 1, false)
+  WENC_GEMM_CASE(128, 2, false)
+  WENC_GEMM_CASE(256, 0, true)
+  WENC_GEMM_CASE(256, 1, true)
+  WENC_GEMM_CASE(256, 2, true)
+  WENC_GEMM_CASE(128, 0, true)
+  WENC_GEMM_CASE(128, 1, true)
+  WENC_GEMM_CASE(128, 2, true)
 #undef WENC_GEMM_CASE
   return cudaErrorInvalidValue;
 }

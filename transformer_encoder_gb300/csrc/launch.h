@@ -34,15 +34,23 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 // box_inner x box_outer elements, 128-byte swizzled (box_inner * 2 must be 128).
 bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                        uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, std::string* why);
+// 2-D fp32 view, box box_inner x box_outer (box_inner * 4 must be 128).
+bool make_tmap_2d_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
+                      uint32_t box_inner, uint32_t box_outer, std::string* why);
 // 3-D bf16 view [dim2][dim1][inner] with explicit strides (bytes) for dims 1 and 2.
 bool make_tmap_3d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t dim1, uint64_t dim2,
                        uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box_inner, uint32_t box1,
                        std::string* why);
+// The same over fp32 elements (box_inner * 4 must be 128).
+bool make_tmap_3d_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t dim1, uint64_t dim2,
+                      uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box_inner, uint32_t box1,
+                      std::string* why);
 
 // ---------------------------------------------------------------- LayerNorm
 bool layernorm_supported(int d);
+// out_fmt: 0 = fp32, 1 = bf16, 2 = fp32 rounded to TF32.
 cudaError_t launch_layernorm(const float* x, const float* w, const float* b, void* y, int rows, int d, float eps,
-                             bool out_bf16, cudaStream_t stream);
+                             int out_fmt, cudaStream_t stream);
 
 // ---------------------------------------------------------------- GEMM (tcgen05)
 // C[M, N] = A[M, K] * W[N, K]^T with a fused epilogue (wenc_epilogue values).
@@ -50,9 +58,12 @@ cudaError_t launch_layernorm(const float* x, const float* w, const float* b, voi
 int gemm_pick_bn(int N);  // 0 if N is unsupported
 constexpr int kGemmBM = 128;
 constexpr int kGemmBK = 64;
+// tf32 = false: bf16 A and W (maps with box 64 x rows), epilogues 0, 1, 2.
+// tf32 = true: fp32 A and W read as TF32 (maps with box 32 x rows); epilogues 0 and 1 write
+// fp32 rounded to TF32 instead of bf16. K must be a multiple of 64 (bf16) or 32 (TF32).
 cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmW, int M, int N, int K, int bn, int epilogue,
                         const float* bias, const float* resid, void* out, uint32_t* err, int num_sms,
-                        cudaStream_t stream);
+                        cudaStream_t stream, bool tf32 = false);
 
 // ---------------------------------------------------------------- attention (tcgen05)
 // Q/K/V tiles are read through 3-D maps [B][T][row] (box 64 x 128 elements for all three);
@@ -79,7 +90,18 @@ cudaError_t launch_attention_combine(const float* part_o, const float2* part_ml,
                                      int T, int H, int n_splits, cudaStream_t stream);
 int attention_launches(int T, int n_splits);  // kernels one launch_attention makes (1 or 2)
 
+// TF32 attention: Q/K/V fp32 [B][T][row] through 3-D fp32 maps (box 32 x 128 for Q, 32 x
+// kAttnTf32BKV for K and V; each 64-wide head is read as two 32-column boxes); out fp32
+// rounded to TF32, row (b*T+t) at out + (b*T+t)*out_stride + 64h. One CTA per 128 queries.
+constexpr int kAttnTf32BQ = 128;
+constexpr int kAttnTf32BKV = 64;
+cudaError_t launch_attention_tf32(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, int q_col0,
+                                  int k_col0, int v_col0, float* out, int out_stride, int B, int T, int H,
+                                  uint32_t* err, cudaStream_t stream);
+
 // ---------------------------------------------------------------- weight packing
 cudaError_t launch_f32_to_bf16(const float* src, uint16_t* dst, size_t n, cudaStream_t stream);
+// fp32 (rounded to TF32, nearest, ties away) or bf16 (widened, exact) -> fp32 for the TF32 path.
+cudaError_t launch_to_tf32(const void* src, bool src_bf16, float* dst, size_t n, cudaStream_t stream);
 
 }  // namespace wenc_host

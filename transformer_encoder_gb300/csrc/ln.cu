@@ -8,7 +8,8 @@
 // One warp per row: the row is read once from HBM with coalesced 16-byte loads and kept in
 // registers, the mean and then the sum of squared deviations are reduced with shuffles (two
 // passes over registers, one pass over memory), and the output is written as bf16 (feeding
-// the next GEMM's TMA loads: LayerNorm and the operand cast fused) or fp32 (the final LN).
+// the next GEMM's TMA loads: LayerNorm and the operand cast fused), as fp32 rounded to TF32
+// (the same for a TF32 GEMM) or as plain fp32 (the final LN).
 #include <cuda_bf16.h>
 
 #include "launch.h"
@@ -24,8 +25,8 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// NV = d / 128: float4 loads per lane.
-template <int NV, bool OUT_BF16>
+// NV = d / 128: float4 loads per lane. OUT: 0 = fp32, 1 = bf16, 2 = fp32 rounded to TF32.
+template <int NV, int OUT>
 __global__ void __launch_bounds__(32 * kRowsPerBlock)
     layernorm_kernel(const float* __restrict__ x, const float* __restrict__ w, const float* __restrict__ b,
                      void* __restrict__ y, int rows, float eps) {
@@ -62,24 +63,27 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock)
     o.y = (v[i].y - mean) * rstd * ww.y + bb.y;
     o.z = (v[i].z - mean) * rstd * ww.z + bb.z;
     o.w = (v[i].w - mean) * rstd * ww.w + bb.w;
-    if constexpr (OUT_BF16) {
+    if constexpr (OUT == 1) {
       uint2 pk = make_uint2(wenc_dev::pack_bf16x2(o.x, o.y), wenc_dev::pack_bf16x2(o.z, o.w));
       reinterpret_cast<uint2*>(static_cast<uint16_t*>(y) + static_cast<size_t>(row) * D)[c4] = pk;
     } else {
+      if constexpr (OUT == 2) {
+        o.x = wenc_dev::round_tf32(o.x); o.y = wenc_dev::round_tf32(o.y);
+        o.z = wenc_dev::round_tf32(o.z); o.w = wenc_dev::round_tf32(o.w);
+      }
       reinterpret_cast<float4*>(static_cast<float*>(y) + static_cast<size_t>(row) * D)[c4] = o;
     }
   }
 }
 
 template <int NV>
-cudaError_t launch_nv(const float* x, const float* w, const float* b, void* y, int rows, float eps, bool out_bf16,
+cudaError_t launch_nv(const float* x, const float* w, const float* b, void* y, int rows, float eps, int out_fmt,
                       cudaStream_t stream) {
   const int grid = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
-  if (out_bf16)
-    return wenc_host::launch_pdl(layernorm_kernel<NV, true>, dim3(grid), dim3(32 * kRowsPerBlock), 0, stream, x, w, b,
-                                 y, rows, eps);
-  return wenc_host::launch_pdl(layernorm_kernel<NV, false>, dim3(grid), dim3(32 * kRowsPerBlock), 0, stream, x, w, b, y,
-                               rows, eps);
+  const dim3 block(32 * kRowsPerBlock);
+  if (out_fmt == 1) return wenc_host::launch_pdl(layernorm_kernel<NV, 1>, dim3(grid), block, 0, stream, x, w, b, y, rows, eps);
+  if (out_fmt == 2) return wenc_host::launch_pdl(layernorm_kernel<NV, 2>, dim3(grid), block, 0, stream, x, w, b, y, rows, eps);
+  return wenc_host::launch_pdl(layernorm_kernel<NV, 0>, dim3(grid), block, 0, stream, x, w, b, y, rows, eps);
 }
 
 __global__ void f32_to_bf16_kernel(const float* __restrict__ src, uint16_t* __restrict__ dst, size_t n) {
@@ -90,6 +94,18 @@ __global__ void f32_to_bf16_kernel(const float* __restrict__ src, uint16_t* __re
   }
 }
 
+// Weight packing for the TF32 path: fp32 matrices are rounded to TF32 (nearest, ties away
+// from zero); bf16 matrices are widened, which is exact (bf16 has fewer mantissa bits).
+__global__ void to_tf32_kernel(const void* __restrict__ src, int src_bf16, float* __restrict__ dst, size_t n) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    if (src_bf16)
+      dst[i] = __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t*>(src)[i]) << 16);
+    else
+      dst[i] = wenc_dev::round_tf32(static_cast<const float*>(src)[i]);
+  }
+}
+
 }  // namespace
 
 namespace wenc_host {
@@ -97,11 +113,12 @@ namespace wenc_host {
 bool layernorm_supported(int d) { return d > 0 && d % 128 == 0 && d / 128 <= 16; }
 
 cudaError_t launch_layernorm(const float* x, const float* w, const float* b, void* y, int rows, int d, float eps,
-                             bool out_bf16, cudaStream_t stream) {
+                             int out_fmt, cudaStream_t stream) {
+  if (out_fmt < 0 || out_fmt > 2) return cudaErrorInvalidValue;
   if (rows <= 0) return cudaSuccess;
   switch (d / 128) {
 #define WENC_LN_CASE(N) \
-  case N: return launch_nv<N>(x, w, b, y, rows, eps, out_bf16, stream);
+  case N: return launch_nv<N>(x, w, b, y, rows, eps, out_fmt, stream);
     WENC_LN_CASE(1) WENC_LN_CASE(2) WENC_LN_CASE(3) WENC_LN_CASE(4) WENC_LN_CASE(5) WENC_LN_CASE(6)
     WENC_LN_CASE(7) WENC_LN_CASE(8) WENC_LN_CASE(9) WENC_LN_CASE(10) WENC_LN_CASE(11) WENC_LN_CASE(12)
     WENC_LN_CASE(13) WENC_LN_CASE(14) WENC_LN_CASE(15) WENC_LN_CASE(16)
@@ -114,6 +131,13 @@ cudaError_t launch_f32_to_bf16(const float* src, uint16_t* dst, size_t n, cudaSt
   if (n == 0) return cudaSuccess;
   const size_t blocks = (n + 255) / 256;
   f32_to_bf16_kernel<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(src, dst, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_to_tf32(const void* src, bool src_bf16, float* dst, size_t n, cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  const size_t blocks = (n + 255) / 256;
+  to_tf32_kernel<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(src, src_bf16 ? 1 : 0, dst, n);
   return cudaGetLastError();
 }
 

@@ -11,14 +11,17 @@ import ctypes
 import os
 
 __all__ = [
-    "WencError", "lib", "lib_path", "Encoder", "attention", "layernorm", "linear", "sync_status",
-    "EPI_BIAS_BF16", "EPI_BIAS_GELU_BF16", "EPI_BIAS_RESID_F32", "EXPORTED_SYMBOLS",
+    "WencError", "lib", "lib_path", "Encoder", "attention", "attention_tf32", "layernorm", "linear", "linear_tf32",
+    "sync_status", "EPI_BIAS_BF16", "EPI_BIAS_GELU_BF16", "EPI_BIAS_RESID_F32", "LN_OUT_F32", "LN_OUT_BF16",
+    "LN_OUT_TF32", "PREC_BF16", "PREC_TF32", "EXPORTED_SYMBOLS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 lib_path = os.path.join(_PKG, "_lib", "libwenc.so")
 
 EPI_BIAS_BF16, EPI_BIAS_GELU_BF16, EPI_BIAS_RESID_F32 = 0, 1, 2
+LN_OUT_F32, LN_OUT_BF16, LN_OUT_TF32 = 0, 1, 2
+PREC_BF16, PREC_TF32 = 0, 1
 _STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "OOM", 4: "CUDA", 5: "DEVICE_TIMEOUT"}
 LAUNCH_KINDS = {0: "layernorm", 1: "gemm_qkv", 2: "attention", 3: "gemm_out", 4: "gemm_fc1", 5: "gemm_fc2",
                 6: "layernorm_final", 7: "copy", 8: "attention_combine"}
@@ -27,6 +30,7 @@ EXPORTED_SYMBOLS = (
     "wenc_create", "wenc_forward", "wenc_forward_layers", "wenc_forward_launches", "wenc_set_launch_events",
     "wenc_attention", "wenc_layernorm", "wenc_linear", "wenc_sync_status", "wenc_destroy", "wenc_last_error",
     "wenc_version", "wenc_selftest_wait_timeout", "wenc_attention_static", "wenc_attention_static_capacity",
+    "wenc_linear_tf32", "wenc_attention_tf32",
 )
 
 
@@ -69,6 +73,8 @@ def lib() -> ctypes.CDLL:
         L.wenc_attention.argtypes = [vp, vp, vp, vp, i, i, i, i, vp]
         L.wenc_layernorm.argtypes = [vp, vp, vp, vp, i, i, f, i, vp]
         L.wenc_linear.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, vp]
+        L.wenc_linear_tf32.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, vp]
+        L.wenc_attention_tf32.argtypes = [vp, vp, vp, vp, i, i, i, i, vp]
         L.wenc_sync_status.argtypes = [vp]
         L.wenc_selftest_wait_timeout.argtypes = [vp]
         L.wenc_attention_static.argtypes = [vp, vp, vp, vp, i, i, i, i, vp]
@@ -81,7 +87,7 @@ def lib() -> ctypes.CDLL:
         L.wenc_version.restype = ctypes.c_char_p
         for name in ("wenc_create", "wenc_forward", "wenc_forward_layers", "wenc_set_launch_events", "wenc_attention",
                      "wenc_layernorm", "wenc_linear", "wenc_sync_status", "wenc_forward_launches",
-                     "wenc_selftest_wait_timeout"):
+                     "wenc_selftest_wait_timeout", "wenc_linear_tf32", "wenc_attention_tf32"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -118,11 +124,12 @@ class Encoder:
 
     ``layers`` is a list of dicts with the keys of ``synth.LAYER_KEYS`` holding CUDA tensors
     (matrices float32 or bfloat16 [n_out, n_in], vectors float32). The library copies and
-    packs them, so they may be freed after construction.
+    packs them, so they may be freed after construction. ``precision`` is "bf16" (bf16
+    tensor-core operands) or "tf32" (TF32 operands, fp32 activations).
     """
 
     def __init__(self, layers, n_heads: int, seq_len: int, max_batch: int, final=None, ln_eps: float = 1e-5,
-                 stream=None):
+                 stream=None, precision: str = "bf16"):
         import torch
         L = lib()
         d = layers[0]["wq"].shape[0]
@@ -130,8 +137,11 @@ class Encoder:
         mdtype = layers[0]["wq"].dtype
         if mdtype not in (torch.float32, torch.bfloat16):
             raise TypeError("weight matrices must be float32 or bfloat16")
+        if precision not in ("bf16", "tf32"):
+            raise ValueError(f"precision must be 'bf16' or 'tf32', got {precision!r}")
         cfg = Config(len(layers), d, n_heads, d // n_heads, f, seq_len, max_batch, 1 if final is not None else 0,
-                     ln_eps, 1 if mdtype == torch.bfloat16 else 0, 0)
+                     ln_eps, 1 if mdtype == torch.bfloat16 else 0, PREC_TF32 if precision == "tf32" else PREC_BF16)
+        self.precision = precision
         arr = (LayerWeights * len(layers))()
         for i, p in enumerate(layers):
             for k in ("wq", "wk", "wv", "wo", "w1", "w2"):
@@ -213,15 +223,20 @@ def attention(q, k, v, out=None, stream=None):
     return out
 
 
-def layernorm(x, w, b, eps: float = 1e-5, out_bf16: bool = True, out=None, stream=None):
-    """LayerNorm over the last axis of a float32 CUDA tensor; bf16 or float32 output."""
+def layernorm(x, w, b, eps: float = 1e-5, out_bf16: bool = True, out=None, stream=None, out_format=None):
+    """LayerNorm over the last axis of a float32 CUDA tensor.
+
+    Output bf16 (``out_bf16``) or float32; ``out_format`` (LN_OUT_*) overrides it and also
+    offers float32 rounded to TF32.
+    """
     import torch
     _require(x, torch.float32, "x")
+    fmt = (LN_OUT_BF16 if out_bf16 else LN_OUT_F32) if out_format is None else int(out_format)
     d = x.shape[-1]
     rows = x.numel() // d
     if out is None:
-        out = torch.empty(x.shape, dtype=torch.bfloat16 if out_bf16 else torch.float32, device=x.device)
-    _check(lib().wenc_layernorm(_ptr(x), _ptr(w), _ptr(b), _ptr(out), rows, d, eps, int(out_bf16), _stream(stream)))
+        out = torch.empty(x.shape, dtype=torch.bfloat16 if fmt == LN_OUT_BF16 else torch.float32, device=x.device)
+    _check(lib().wenc_layernorm(_ptr(x), _ptr(w), _ptr(b), _ptr(out), rows, d, eps, fmt, _stream(stream)))
     return out
 
 
@@ -237,6 +252,38 @@ def linear(a, w, bias, epilogue: int = EPI_BIAS_BF16, resid=None, out=None, stre
         dt = torch.float32 if epilogue == EPI_BIAS_RESID_F32 else torch.bfloat16
         out = torch.empty((M, N), dtype=dt, device=a.device)
     _check(lib().wenc_linear(_ptr(a), _ptr(w), _ptr(bias), _ptr(resid), _ptr(out), M, N, K, epilogue, _stream(stream)))
+    return out
+
+
+def linear_tf32(a, w, bias, epilogue: int = EPI_BIAS_BF16, resid=None, out=None, stream=None):
+    """out = epilogue(a w^T + bias) on TF32 tensor cores; a float32 [M, K], w float32 [N, K].
+
+    Epilogues 0 and 1 write float32 rounded to TF32, epilogue 2 float32 (resid + product).
+    """
+    import torch
+    _require(a, torch.float32, "a")
+    _require(w, torch.float32, "w")
+    _require(bias, torch.float32, "bias")
+    M, K = a.shape
+    N = w.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=a.device)
+    _require(out, torch.float32, "out")
+    _check(lib().wenc_linear_tf32(_ptr(a), _ptr(w), _ptr(bias), _ptr(resid), _ptr(out), M, N, K, epilogue,
+                                  _stream(stream)))
+    return out
+
+
+def attention_tf32(q, k, v, out=None, stream=None):
+    """out = softmax(q k^T / 8) v per (window, head) with TF32 products; float32 [B, T, H, 64]."""
+    import torch
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _require(t, torch.float32, n)
+    B, T, H, hd = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _require(out, torch.float32, "out")
+    _check(lib().wenc_attention_tf32(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, T, H, hd, _stream(stream)))
     return out
 
 
