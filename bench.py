@@ -2,6 +2,7 @@
 """Throughput of the Whisper encoder stack on GB300: 30 s windows per second and TFLOP/s.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload large_stack] [--impl wenc|reference]
+                    [--precision bf16|tf32]
 
 A step is one wenc_forward call over one batch of synthetic windows (all blocks + the final
 LayerNorm). Default workload: the large-dims stack (32 blocks, batch 16, T 1500, d 1280,
@@ -10,6 +11,9 @@ LayerNorm). Default workload: the large-dims stack (32 blocks, batch 16, T 1500,
 same C-ABI call with the input copied from pinned host memory and the output copied back
 inside the timed region. Multi-GPU runs are independent replicas (windows are independent;
 there is no collective on the data path): value = all ranks' windows / the slowest rank's time.
+
+`--precision tf32` runs the same step with TF32 tensor-core operands and fp32 activations; its
+roofline peak is the measured bf16 peak times the nominal TF32/BF16 ratio (1.1 / 2.25 PFLOP/s).
 
 `--impl reference` times the f64 CPU oracle (the only other implementation) on the host
 cores on a bounded sample of the same workload (one block of one window per step) and
@@ -32,6 +36,7 @@ if ROOT not in sys.path:
 
 METRIC = "encoder 30s-windows/sec and TFLOP/s (% of BF16 peak) at 1 GB300"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+TF32_PER_BF16 = 1.1 / 2.25  # nominal dense tensor-core rates of GB300 (PFLOP/s)
 
 
 def load_peaks():
@@ -43,30 +48,49 @@ def load_peaks():
     return dict(PEAKS_FALLBACK), "fallback"
 
 
-def kernel_source_hash() -> str:
-    """sha256 over the CUDA sources and headers of libwenc (identifies the profiled build)."""
+# The source files each profiled kernel is built from (plus the shared headers). A traffic
+# figure is reported only while these files are byte-identical to the profiled ones.
+KERNEL_SOURCES = {
+    "gemm": ("gemm.cu",),
+    "attention": ("attn.cu",),
+    "attention_tf32": ("attn_tf32.cu",),
+    "layernorm": ("ln.cu",),
+}
+SHARED_SOURCES = ("ptx.cuh", "launch.h")
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """sha256 over the CUDA sources of one kernel family and the shared device headers."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "transformer_encoder_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            h.update(name.encode())
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(f.read())
-    with open(os.path.join(ROOT, "include", "wenc.h"), "rb") as f:
-        h.update(f.read())
+    for name in (*KERNEL_SOURCES[kernel], *SHARED_SOURCES):
+        h.update(name.encode())
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()
 
 
-def load_traffic():
-    """DRAM bytes per launch measured by ncu (profiles/traffic.json), or None once the kernel
-    sources differ from the ones that were profiled."""
+def _family(launch_name: str, tf32: bool) -> str:
+    if launch_name.startswith("gemm_"):
+        return "gemm"
+    if launch_name == "attention":
+        return "attention_tf32" if tf32 else "attention"
+    return "layernorm"
+
+
+def load_traffic(tf32: bool = False):
+    """DRAM bytes per launch measured by ncu (profiles/traffic.json), for the launches whose
+    kernel sources are still the ones that were profiled; {} when none are."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
-        return None
+        return {}
     with open(p) as f:
         d = json.load(f)
-    return d if d.get("source_sha256") == kernel_source_hash() else None
+    hashes = d.get("source_sha256", {})
+    per = d.get("bytes_per_launch_tf32" if tf32 else "bytes_per_launch", {})
+    return {k: v for k, v in per.items()
+            if hashes.get(_family(k, tf32)) == kernel_source_hash(_family(k, tf32))}
 
 
 def combine_rank_timings(ms_total: float, ms_e2e: float, world: int, device="cuda"):
@@ -251,7 +275,8 @@ def run_wenc(args, w):
 
     _, final, rng = synth.make_weights(w, layer_callback=lambda p: dev_layers.append(up(p)))
     fin = (torch.from_numpy(final[0]).cuda(), torch.from_numpy(final[1]).cuda()) if w.final_ln else None
-    enc = Encoder(dev_layers, w.n_heads, w.seq_len, w.batch, final=fin)
+    enc = Encoder(dev_layers, w.n_heads, w.seq_len, w.batch, final=fin, precision=args.precision)
+    tf32 = args.precision == "tf32"
     del dev_layers
     torch.cuda.empty_cache()
     x_host = torch.from_numpy(synth.make_input(w, rng)).pin_memory()
@@ -334,7 +359,7 @@ def run_wenc(args, w):
     gemm_flops = {"gemm_qkv": 2.0 * M * 3 * d * d, "gemm_out": 2.0 * M * d * d,
                   "gemm_fc1": 2.0 * M * f * d, "gemm_fc2": 2.0 * M * d * f}
     attn_flops = 4.0 * w.batch * H * T * T * w.head_dim
-    ln_bytes = 6.0 * M * d
+    ln_bytes = (8.0 if tf32 else 6.0) * M * d  # fp32 read + bf16 or fp32 write
     kern = {}
     for name, (ms, n) in per_kind.items():
         avg = ms / n
@@ -353,28 +378,31 @@ def run_wenc(args, w):
     g_flops_per_launch = sum(gemm_flops[k] * per_kind[k][1] for k in gemm_flops if k in per_kind) / g_n
     g_achieved = g_flops_per_launch / (g_ms / g_n / 1e3) / 1e12
     peak = peaks.get("bf16_tflops_sustained", PEAKS_FALLBACK["bf16_tflops_sustained"])
-    traffic = load_traffic() if w.name in ("large_stack", "large_block") else None
+    peak_name = "bf16_tflops_sustained"
+    if tf32:
+        peak *= TF32_PER_BF16
+        peak_name = "bf16_tflops_sustained x 1.1/2.25 (nominal TF32/BF16)"
+    per = load_traffic(tf32) if w.name in ("large_stack", "large_block") else {}
     g_traffic = None
-    if traffic is not None:
-        per = traffic["bytes_per_launch"]
+    if per:
         for name in kern:
             if name in per:
                 kern[name]["traffic_bytes"] = per[name]
         if all(k in per for k in gemm_flops):
             g_traffic = sum(per[k] * per_kind[k][1] for k in gemm_flops) / g_n
-    roofline = {"kernel": "gemm_tc_kernel (QKV, out-proj, fc1, fc2 launches)", "bound": "tensor",
-                "achieved": g_achieved, "peak": peak, "unit": "TFLOP/s", "frac": g_achieved / peak,
-                "peak_source": f"bf16_tflops_sustained, {peak_src}", "traffic": g_traffic,
+    roofline = {"kernel": f"gemm_tc_kernel{' (TF32)' if tf32 else ''} (QKV, out-proj, fc1, fc2 launches)",
+                "bound": "tensor", "achieved": g_achieved, "peak": peak, "unit": "TFLOP/s", "frac": g_achieved / peak,
+                "peak_source": f"{peak_name}, {peak_src}", "traffic": g_traffic,
                 "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)"}
 
     line = {
         "metric": METRIC, "value": value, "unit": "windows/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": "tf32" if tf32 else "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(w), "windows_per_step": w.batch, "seq_len": T,
                    "l2": "no flush: each step streams 1.26 GB of weights and >400 MB of activations, above the 126 MB L2"
                    if w.name == "large_stack" else "no flush",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}", "precision": args.precision},
         "tflops": tflops,
         "pct_of_bf16_peak": {"burst": 100 * tflops / world / peaks["bf16_tflops"],
                              "sustained": 100 * tflops / world / peaks["bf16_tflops_sustained"],
@@ -406,6 +434,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="large_stack")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle's CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--precision", choices=("bf16", "tf32"), default="bf16",
+                    help="tensor-core operand precision of the timed path")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "wenc":
         print("note: warm-up raised to the minimum of 3 steps", file=sys.stderr)

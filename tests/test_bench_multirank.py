@@ -55,8 +55,21 @@ def test_traffic_figures_track_the_kernel_sources():
     import json
 
     import bench
-    t = bench.load_traffic()
     with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-        recorded = json.load(f)["source_sha256"]
-    # Either the sources are the profiled ones (figures reported) or they changed (null).
-    assert (t is not None) == (recorded == bench.kernel_source_hash())
+        d = json.load(f)
+    recorded = d["source_sha256"]
+    for tf32, key in ((False, "bytes_per_launch"), (True, "bytes_per_launch_tf32")):
+        got = bench.load_traffic(tf32)
+        for name in d.get(key, {}):
+            fam = bench._family(name, tf32)
+            # a figure is reported exactly while its kernel's sources are the profiled ones
+            assert (name in got) == (recorded.get(fam) == bench.kernel_source_hash(fam)), (name, tf32)
+
+
+def test_traffic_gate_drops_a_changed_kernel(monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    real = bench.kernel_source_hash
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda k: "changed" if k == "attention" else real(k))
+    got = bench.load_traffic(False)
+    assert "attention" not in got

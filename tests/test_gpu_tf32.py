@@ -61,7 +61,7 @@ def test_linear_tf32_matches_oracle(M, N, K, epi):
     """Operands on the TF32 grid; the product is exact in fp32, accumulation adds at most
     2^-16 of sum |a||w| here; epilogues 0 and 1 add one TF32 rounding of the output."""
     import torch
-    from transformer_encoder_gb300 import linear_tf32
+    from transformer_encoder_gb300 import linear_tf32, sync_status
     rng = np.random.default_rng(M + N + K + 10 * epi)
     a = synth.round_to_tf32(rng.standard_normal((M, K)).astype(np.float32))
     wt = synth.round_to_tf32((0.05 * rng.standard_normal((N, K))).astype(np.float32))
@@ -69,6 +69,7 @@ def test_linear_tf32_matches_oracle(M, N, K, epi):
     resid = rng.standard_normal((M, N)).astype(np.float32) if epi == 2 else None
     out = linear_tf32(_t(a), _t(wt), _t(bias), epi, resid=_t(resid) if resid is not None else None)
     torch.cuda.synchronize()
+    sync_status()
     z = oracle.linear(a, wt, bias)
     absz = np.abs(a.astype(np.float64)) @ np.abs(wt.astype(np.float64)).T
     acc = 2.0 ** -16 * absz + 1e-6
@@ -101,10 +102,11 @@ def _attn_case(B, T, H, scale, seed):
 @pytest.mark.parametrize("scale", [1.0, 0.1])
 def test_attention_tf32_matches_oracle(B, T, H, scale):
     import torch
-    from transformer_encoder_gb300 import attention_tf32
+    from transformer_encoder_gb300 import attention_tf32, sync_status
     (tq, tk, tv), (q, k, v) = _attn_case(B, T, H, scale, seed=3 + T + H)
     out = attention_tf32(tq, tk, tv)
     torch.cuda.synchronize()
+    sync_status()  # no bounded wait of the kernel ran out
     assert _on_tf32_grid(out)
     got = out.cpu().numpy().astype(np.float64).reshape(B, T, H * 64)
     attention_gate(got, q, k, v, H, what=f"TF32 attention B={B} T={T} H={H} scale={scale}", tf32=True)

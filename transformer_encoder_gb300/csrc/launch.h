@@ -92,7 +92,7 @@ int attention_launches(int T, int n_splits);  // kernels one launch_attention ma
 
 // TF32 attention: Q/K/V fp32 [B][T][row] through 3-D fp32 maps (box 32 x 128 for Q, 32 x
 // kAttnTf32BKV for K and V; each 64-wide head is read as two 32-column boxes); out fp32
-// rounded to TF32, row (b*T+t) at out + (b*T+t)*out_stride + 64h. One CTA per 128 queries.
+// rounded to TF32, row (b*T+t) at out + (b*T+t)*out_stride + 64h. One CTA per 2 x 128 queries.
 constexpr int kAttnTf32BQ = 128;
 constexpr int kAttnTf32BKV = 64;
 cudaError_t launch_attention_tf32(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, int q_col0,
