@@ -19,6 +19,10 @@ beyond what the definition states. Sources, by page and section:
 * "oxinfer 0.0.5 src/whisper/model.rs": ``WhisperModel::encode`` (the same
   block with ``LN_EPS = 1e-5``, non-causal attention, final ``enc_ln``).
 
+``oracle.stem`` adds the convolutional stem in front of the blocks (conv1 and conv2
+with exact-erf GELU, then the positional rows), from turbospark-runtime
+``encode_partial`` and oxinfer ``WhisperModel::encode``.
+
 Parity pins live in ``tests/test_oracle_pins.py``: hand-worked cases under
 ``tests/golden/``, closed forms, invariants and a cross-check against
 PyTorch's float64 CPU ``TransformerEncoderLayer`` (norm_first, erf GELU).
@@ -27,3 +31,4 @@ from .encoder import (  # noqa: F401
     layer_norm, linear, gelu, softmax_rows, attention, attention_online,
     encoder_block, encoder_stack, block_rows, LN_EPS,
 )
+from .stem import conv1d, conv_stem  # noqa: F401

@@ -31,7 +31,7 @@ import numpy as np
 __all__ = [
     "Workload", "WORKLOADS", "LAYER_KEYS", "MATRIX_KEYS",
     "f32_to_bf16_bits", "bf16_bits_to_f32", "round_to_bf16", "round_to_tf32",
-    "make_layer", "make_weights", "make_input", "make_qkv",
+    "make_layer", "make_weights", "make_input", "make_qkv", "make_stem", "make_mel",
 ]
 
 T_WINDOW = 1500  # encoder positions of one zero-padded 30 s window
@@ -54,6 +54,7 @@ class Workload:
     seq_len: int = T_WINDOW
     seed: int = 0
     head_dim: int = field(default=64)
+    n_mels: int = 80  # mel bands of the convolutional stem's input (128 for large-v3)
 
     @property
     def rows(self) -> int:
@@ -71,10 +72,10 @@ WORKLOADS = {
     "tiny_stack": Workload("tiny_stack", 1, 384, 6, 1536, 4, final_ln=True, bf16_weights=True),
     "base_stack": Workload("base_stack", 4, 512, 8, 2048, 6, final_ln=True, bf16_weights=True),
     "small_stack": Workload("small_stack", 8, 768, 12, 3072, 12, final_ln=True, bf16_weights=True),
-    "large_stack": Workload("large_stack", 16, 1280, 20, 5120, 32, final_ln=True, bf16_weights=True),
+    "large_stack": Workload("large_stack", 16, 1280, 20, 5120, 32, final_ln=True, bf16_weights=True, n_mels=128),
     # One block at large-v3 dims and batch 16: every kernel launch has exactly the shape it has
     # inside the 32-block stack, with ~1 GB on the device (used for profiler captures).
-    "large_block": Workload("large_block", 16, 1280, 20, 5120, 1, final_ln=True, bf16_weights=True),
+    "large_block": Workload("large_block", 16, 1280, 20, 5120, 1, final_ln=True, bf16_weights=True, n_mels=128),
 }
 
 
@@ -151,6 +152,36 @@ def make_input(w: Workload, rng: np.random.Generator, batch: int | None = None) 
     """Hidden states [B, T, d] ~ N(0, 1), float32 (drawn after all parameters)."""
     b = w.batch if batch is None else batch
     return rng.standard_normal((b, w.seq_len, w.d_model), dtype=np.float32)
+
+
+STEM_SEED_OFFSET = 7919  # the stem draws from a generator of its own (block draws unchanged)
+
+
+def make_stem(w: Workload) -> dict:
+    """Convolutional-stem parameters: conv1_w [d, n_mels, 3], conv2_w [d, d, 3] (checkpoint
+    layout), conv biases [d], and the positional table [seq_len, d].
+
+    Matrices ~ N(0, 0.02) (rounded to bf16 for bf16 workloads), biases ~ N(0, 0.01), positions
+    ~ U(-1, 1) (the value range of Whisper's sinusoidal table), from PCG64(seed + 7919).
+    """
+    rng = np.random.Generator(np.random.PCG64(w.seed + STEM_SEED_OFFSET))
+    mat = (lambda shape: round_to_bf16(_normal(rng, shape, 0.02))) if w.bf16_weights else (lambda shape: _normal(rng, shape, 0.02))
+    d = w.d_model
+    p = {}
+    p["conv1_w"] = mat((d, w.n_mels, 3))
+    p["conv1_b"] = _normal(rng, (d,), 0.01)
+    p["conv2_w"] = mat((d, d, 3))
+    p["conv2_b"] = _normal(rng, (d,), 0.01)
+    p["positions"] = rng.uniform(-1.0, 1.0, (w.seq_len, d)).astype(np.float32)
+    return p
+
+
+def make_mel(w: Workload, batch: int | None = None, seed: int = 2) -> np.ndarray:
+    """Log-mel windows [B, 2 * seq_len, n_mels] (time-major), ~ U(-1, 1): the range of Whisper's
+    normalised log-mel features."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    b = w.batch if batch is None else batch
+    return rng.uniform(-1.0, 1.0, (b, 2 * w.seq_len, w.n_mels)).astype(np.float32)
 
 
 def make_qkv(batch: int, seq: int, heads: int, head_dim: int = 64, seed: int = 1, scale: float = 1.0):

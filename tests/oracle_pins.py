@@ -16,6 +16,7 @@ import os
 import numpy as np
 
 import oracle.encoder as E
+import oracle.stem as S
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
@@ -248,6 +249,66 @@ def pin_block_rows_matches_block():
     x1r, yr = E.block_rows(x, rows, p, H)
     _close(x1r, x1[rows], rtol=1e-12, atol=1e-12)
     _close(yr, y[rows], rtol=1e-12, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------- conv stem
+def pin_conv1d_hand():
+    g = _golden("conv1d_hand.json")
+    _close(S.conv1d(g["x"], g["w"], g["b"], stride=1, pad=1), g["y_stride1_pad1"], rtol=1e-14, atol=1e-15)
+    _close(S.conv1d(g["x"], g["w"], g["b"], stride=2, pad=1), g["y_stride2_pad1"], rtol=1e-14, atol=1e-15)
+
+
+def pin_conv1d_closed_forms():
+    # One tap per kernel: the centre tap copies the input, the first tap delays it by one
+    # frame (zero at t = 0), and stride 2 with the centre tap keeps every other frame.
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((2, 9, 4))
+    b = rng.standard_normal(4)
+    eye = np.eye(4)
+    centre = np.zeros((4, 4, 3))
+    centre[:, :, 1] = eye
+    first = np.zeros((4, 4, 3))
+    first[:, :, 0] = eye
+    _close(S.conv1d(x, centre, b, 1, 1), x + b)
+    delayed = np.concatenate([np.zeros((2, 1, 4)), x[:, :-1]], axis=1)
+    _close(S.conv1d(x, first, b, 1, 1), delayed + b)
+    _close(S.conv1d(x, centre, b, 2, 1), x[:, ::2] + b)
+    # window lengths of the encoder: 3000 mel frames -> 3000 -> 1500 positions
+    assert S.conv1d(np.zeros((3000, 1)), np.zeros((1, 1, 3)), [0.0], 1, 1).shape == (3000, 1)
+    assert S.conv1d(np.zeros((3000, 1)), np.zeros((1, 1, 3)), [0.0], 2, 1).shape == (1500, 1)
+
+
+def pin_conv1d_torch():
+    import torch
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((3, 50, 7))
+    w = rng.standard_normal((5, 7, 3))
+    b = rng.standard_normal(5)
+    for stride in (1, 2):
+        ref = torch.nn.functional.conv1d(torch.from_numpy(x).transpose(1, 2), torch.from_numpy(w),
+                                         torch.from_numpy(b), stride=stride, padding=1).transpose(1, 2).numpy()
+        _close(S.conv1d(x, w, b, stride, 1), ref, rtol=1e-12, atol=1e-12)
+
+
+def pin_conv_stem_torch():
+    # The stem as torch modules: Conv1d(k3, s1, p1) -> exact GELU -> Conv1d(k3, s2, p1) -> exact
+    # GELU -> + positions, on one 2-window batch.
+    import torch
+    rng = np.random.default_rng(13)
+    n_mels, d, n = 6, 5, 8
+    mel = rng.standard_normal((2, 2 * n, n_mels))
+    w1, b1 = rng.standard_normal((d, n_mels, 3)), rng.standard_normal(d)
+    w2, b2 = rng.standard_normal((d, d, 3)), rng.standard_normal(d)
+    pos = rng.standard_normal((n + 3, d))
+    c1 = torch.nn.Conv1d(n_mels, d, 3, stride=1, padding=1).double()
+    c2 = torch.nn.Conv1d(d, d, 3, stride=2, padding=1).double()
+    with torch.no_grad():
+        c1.weight.copy_(torch.from_numpy(w1)); c1.bias.copy_(torch.from_numpy(b1))
+        c2.weight.copy_(torch.from_numpy(w2)); c2.bias.copy_(torch.from_numpy(b2))
+        gelu = torch.nn.GELU()
+        h = gelu(c1(torch.from_numpy(mel).transpose(1, 2)))
+        ref = (gelu(c2(h)).transpose(1, 2) + torch.from_numpy(pos[:n])).numpy()
+    _close(S.conv_stem(mel, w1, b1, w2, b2, pos), ref, rtol=1e-12, atol=1e-12)
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

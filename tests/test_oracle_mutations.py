@@ -8,6 +8,7 @@ import numpy as np
 import pytest
 
 import oracle.encoder as E
+import oracle.stem as S
 import oracle_pins as P
 
 
@@ -101,6 +102,37 @@ def _stack_drops_final(x, layers, n_heads, final=None, eps=E.LN_EPS):
     return y
 
 
+def _conv_flipped(x, w, b, stride, pad):
+    # a true convolution (kernel reversed) instead of the layer's cross-correlation
+    return _CONV(x, np.asarray(w, np.float64)[:, :, ::-1], b, stride, pad)
+
+
+def _conv_channels_swapped(x, w, b, stride, pad):
+    w = np.asarray(w, np.float64)
+    return _CONV(x, np.swapaxes(w, 0, 1) if w.shape[0] == w.shape[1] else w, b, stride, pad)
+
+
+def _conv_pad_right_only(x, w, b, stride, pad):
+    # all the padding after the window: taps at t, t+1, t+2 instead of t-1, t, t+1
+    x = np.asarray(x, np.float64)
+    xp = np.concatenate([x, np.zeros(x.shape[:-2] + (2 * pad, x.shape[-1]))], axis=-2)
+    return _CONV(xp, w, b, stride, 0)
+
+
+def _stem_variant(kind):
+    def stem(mel, w1, b1, w2, b2, positions):
+        h = E.gelu(S.conv1d(mel, w1, b1, stride=2 if kind == "conv1_strided" else 1, pad=1))
+        y = S.conv1d(h, w2, b2, stride=2, pad=1)
+        pos = np.asarray(positions, np.float64)[: y.shape[-2]]
+        if kind == "gelu_after_positions":
+            return E.gelu(y + pos)
+        y = E.gelu(y)
+        return y if kind == "no_positions" else y + pos
+    return stem
+
+
+_CONV = S.conv1d
+
 MUTATIONS = {
     "ln_unbiased_variance": ("layer_norm", _ln_unbiased),
     "ln_missing_eps": ("layer_norm", _ln_no_eps),
@@ -121,13 +153,22 @@ MUTATIONS = {
     "block_no_gelu": ("encoder_block", _block_variant("no_gelu")),
     "block_no_ffn_residual": ("encoder_block", _block_variant("no_ffn_residual")),
     "stack_drops_final_ln": ("encoder_stack", _stack_drops_final),
+    "conv_kernel_flipped": ("S.conv1d", _conv_flipped),
+    "conv_channels_swapped": ("S.conv1d", _conv_channels_swapped),
+    "conv_padding_one_sided": ("S.conv1d", _conv_pad_right_only),
+    "stem_no_positions": ("S.conv_stem", _stem_variant("no_positions")),
+    "stem_gelu_after_positions": ("S.conv_stem", _stem_variant("gelu_after_positions")),
+    "stem_conv1_strided": ("S.conv_stem", _stem_variant("conv1_strided")),
 }
 
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
 def test_mutation_is_caught(name, monkeypatch):
     attr, fn = MUTATIONS[name]
-    monkeypatch.setattr(E, attr, fn)
+    module = E
+    if attr.startswith("S."):
+        module, attr = S, attr[2:]
+    monkeypatch.setattr(module, attr, fn)
     caught = []
     for pin in P.ALL_PINS:
         try:
