@@ -108,6 +108,18 @@ typedef struct {
   const void* w2; const float* b2;
 } wenc_layer_weights;
 
+/* The convolutional stem in front of the blocks (optional; see wenc_set_stem). Device
+ * pointers owned by the caller. Matrices in config.weight_dtype with the checkpoint layout
+ * [C_out, C_in, 3]; vectors float32. */
+typedef struct {
+  int n_mels;             /* mel bands of the input: a multiple of 8, 8..1024 (80; 128 for large-v3) */
+  const void* conv1_w;    /* [d, n_mels, 3]: kernel 3, stride 1, padding 1 */
+  const float* conv1_b;   /* [d] */
+  const void* conv2_w;    /* [d, d, 3]: kernel 3, stride 2, padding 1 */
+  const float* conv2_b;   /* [d] */
+  const float* positions; /* [seq_len, d]: row t is added to output position t after conv2's GELU */
+} wenc_stem_weights;
+
 typedef struct wenc wenc; /* opaque handle */
 
 /* wenc_create -- validate `cfg`, pack the weights into library-owned device memory
@@ -138,6 +150,31 @@ WENC_API wenc_status wenc_forward(wenc* h, const float* hidden_in, float* hidden
 WENC_API wenc_status wenc_forward_layers(wenc* h, const float* hidden_in, float* hidden_out, int B,
                                 int first, int count, int apply_final_ln, wenc_stream_t stream);
 
+/* wenc_set_stem -- attach the convolutional stem to a handle (turbospark-runtime
+ * encode_partial's conv front end; oxinfer WhisperModel::encode):
+ *   h = GELU_erf(conv1(mel)),  x = GELU_erf(conv2(h)) + positions,
+ * conv1 kernel 3 / stride 1 / padding 1 (n_mels -> d over 2*seq_len frames), conv2 kernel 3 /
+ * stride 2 / padding 1 (d -> d, 2*seq_len -> seq_len positions). Packs the weights into
+ * library-owned memory in the handle's precision (each convolution runs as one tensor-core GEMM
+ * over the unfolded signal, weights reordered to [C_out, 3*C_in]) and allocates the stem's
+ * workspace for cfg.max_batch windows. A second call replaces the first. Synchronises `stream`
+ * before returning; the caller's buffers may then be freed.
+ * Errors: INVALID_ARG (NULL pointers, n_mels not a multiple of 8 or outside 8..1024), OOM, CUDA. */
+WENC_API wenc_status wenc_set_stem(wenc* h, const wenc_stem_weights* w, wenc_stream_t stream);
+
+/* wenc_stem -- hidden_out = stem(mel): mel float32 [B, 2*seq_len, n_mels] (time-major log-mel
+ * frames, caller-owned), hidden_out float32 [B, seq_len, d]. 1 <= B <= max_batch; buffers
+ * 16-byte aligned; needs wenc_set_stem first (else INVALID_ARG). Stream-ordered, 4 launches. */
+WENC_API wenc_status wenc_stem(wenc* h, const float* mel, float* hidden_out, int B, wenc_stream_t stream);
+
+/* wenc_encode -- the whole encoder from log-mel frames: the stem, every block and (if
+ * configured) the final LayerNorm. mel as for wenc_stem; hidden_out float32 [B, seq_len, d].
+ * The launch-event hook of wenc_set_launch_events covers all wenc_encode_launches() launches. */
+WENC_API wenc_status wenc_encode(wenc* h, const float* mel, float* hidden_out, int B, wenc_stream_t stream);
+
+/* wenc_encode_launches -- kernel launches of one wenc_encode call (-1 without a stem). */
+WENC_API int wenc_encode_launches(const wenc* h);
+
 /* wenc_forward_launches -- number of kernel launches one wenc_forward_layers call with
  * these arguments makes (for launch accounting). Returns -1 on bad arguments. */
 WENC_API int wenc_forward_launches(const wenc* h, int first, int count, int apply_final_ln);
@@ -147,7 +184,8 @@ WENC_API int wenc_forward_launches(const wenc* h, int first, int count, int appl
  * (each a cudaEvent_t created by the caller), for n_events >= launches + 1; the hook
  * then clears itself. kinds (may be NULL) receives, per launch, 0 = LayerNorm,
  * 1 = QKV GEMM, 2 = attention, 3 = out-proj GEMM, 4 = fc1 GEMM, 5 = fc2 GEMM,
- * 6 = final LayerNorm, 7 = copy, 8 = attention split-key merge (small batches only). */
+ * 6 = final LayerNorm, 7 = copy, 8 = attention split-key merge (small batches only),
+ * 9 = stem unfold, 10 = stem conv1 GEMM, 11 = stem conv2 GEMM (wenc_stem, wenc_encode). */
 WENC_API wenc_status wenc_set_launch_events(wenc* h, void* const* events, int n_events, int* kinds);
 
 /* wenc_attention -- out = softmax(q k^T * hd^-0.5) v per (window, head), non-causal,

@@ -94,3 +94,14 @@ def test_host_side_argument_errors_tf32(L):
     assert L.wenc_attention_tf32(p, p, p, p, 1, 0, 2, 64, None) == 1        # T < 1
     assert L.wenc_attention_tf32(p, p, None, p, 1, 10, 2, 64, None) == 1
     assert L.wenc_layernorm(p, p, p, p, 10, 128, 1e-5, 3, None) == 1         # unknown output format
+
+
+def test_host_side_argument_errors_stem(L):
+    from transformer_encoder_gb300.wenc import StemWeights
+    p = ctypes.c_void_p(256)
+    w = StemWeights(80, 256, 256, 256, 256, 256)
+    assert L.wenc_set_stem(None, ctypes.byref(w), None) == 1
+    assert b"handle" in L.wenc_last_error()
+    assert L.wenc_stem(None, p, p, 1, None) == 1
+    assert L.wenc_encode(None, p, p, 1, None) == 1
+    assert L.wenc_encode_launches(None) == -1

@@ -218,6 +218,14 @@ struct wenc {
   // timing hook (one call)
   std::vector<cudaEvent_t> events;
   int* kinds = nullptr;
+  // convolutional stem (wenc_set_stem); weights and workspace in one arena
+  bool has_stem = false;
+  int n_mels = 0, kp1 = 0, bn_stem = 0;
+  void* stem_arena = nullptr;
+  void *wc1 = nullptr, *wc2 = nullptr;  // [d, kp1], [d, 3d] in the operand format
+  float *cb1 = nullptr, *cb2 = nullptr, *pos = nullptr;
+  void *a1 = nullptr, *h1 = nullptr, *a2 = nullptr;  // unfolded mel, conv1 output, unfolded conv1 output
+  CUtensorMap tm_a1, tm_wc1, tm_a2, tm_wc2;
 };
 
 namespace {
@@ -257,6 +265,7 @@ void free_handle(wenc* h) {
   if (!h) return;
   if (h->weight_arena) cudaFree(h->weight_arena);
   if (h->work_arena) cudaFree(h->work_arena);
+  if (h->stem_arena) cudaFree(h->stem_arena);
   if (h->err_host) cudaFreeHost(h->err_host);
   delete h;
 }
@@ -267,6 +276,118 @@ cudaError_t pack_matrix(const void* src, int dtype, bool tf32, void* dst, size_t
   if (tf32) return wenc_host::launch_to_tf32(src, dtype == WENC_DTYPE_BF16, static_cast<float*>(dst), n, s);
   if (dtype == WENC_DTYPE_BF16) return cudaMemcpyAsync(dst, src, n * 2, cudaMemcpyDeviceToDevice, s);
   return wenc_host::launch_f32_to_bf16(static_cast<const float*>(src), static_cast<uint16_t*>(dst), n, s);
+}
+
+}  // namespace
+
+namespace {
+
+// Records each launch's kind and, when the timing hook is armed, an event after it.
+struct LaunchRec {
+  cudaStream_t s;
+  std::vector<cudaEvent_t> ev;
+  int* kinds = nullptr;
+  int li = 0;
+  cudaError_t e = cudaSuccess;
+  void begin() {
+    if (!ev.empty()) e = cudaEventRecord(ev[0], s);
+  }
+  void operator()(int kind, cudaError_t le) {
+    if (e == cudaSuccess) e = le;
+    if (kinds) kinds[li] = kind;
+    ++li;
+    if (!ev.empty() && e == cudaSuccess) e = cudaEventRecord(ev[li], s);
+  }
+};
+
+// Common checks of the forward-type entry points; takes the armed timing hook (which clears it).
+wenc_status begin_call(wenc* h, const void* in, const void* out, int B, int n_launch, cudaStream_t s, LaunchRec* rec) {
+  if (!h) return fail(WENC_ERR_INVALID_ARG, "handle is NULL");
+  if (!in || !out) return fail(WENC_ERR_INVALID_ARG, "input/output buffer is NULL");
+  if (!aligned16(in) || !aligned16(out)) return fail(WENC_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
+  if (B < 1 || B > h->cfg.max_batch)
+    return fail(WENC_ERR_INVALID_ARG, "B = %d outside 1..max_batch %d", B, h->cfg.max_batch);
+  int dev = -1;
+  cudaGetDevice(&dev);
+  if (dev != h->device) return fail(WENC_ERR_INVALID_ARG, "current device %d is not the handle's device %d", dev, h->device);
+  if (*reinterpret_cast<volatile uint32_t*>(h->err_host) != 0)
+    return fail(WENC_ERR_DEVICE_TIMEOUT, "an earlier launch recorded device error word 0x%x",
+                *reinterpret_cast<volatile uint32_t*>(h->err_host));
+  rec->s = s;
+  rec->ev.swap(h->events);
+  h->events.clear();
+  rec->kinds = h->kinds;
+  h->kinds = nullptr;
+  if (!rec->ev.empty() && static_cast<int>(rec->ev.size()) < n_launch + 1)
+    return fail(WENC_ERR_INVALID_ARG, "launch events: need %d, got %zu", n_launch + 1, rec->ev.size());
+  rec->begin();
+  return WENC_OK;
+}
+
+// The stem's four launches: mel [B, 2T, n_mels] -> x [B, T, d] (fp32).
+void enqueue_stem(wenc* h, const float* mel, float* x, int B, LaunchRec& rec) {
+  const wenc_config& c = h->cfg;
+  const int d = c.d_model, T = c.seq_len;
+  rec(9, wenc_host::launch_unfold3(mel, true, h->a1, h->tf32, B, 2 * T, h->n_mels, 1, h->kp1, rec.s));
+  rec(10, wenc_host::launch_gemm(h->tm_a1, h->tm_wc1, B * 2 * T, d, h->kp1, h->bn_stem, WENC_EPI_BIAS_GELU_BF16,
+                                 h->cb1, nullptr, h->h1, h->err_dev, h->num_sms, rec.s, h->tf32));
+  rec(9, wenc_host::launch_unfold3(h->h1, h->tf32, h->a2, h->tf32, B, 2 * T, d, 2, 3 * d, rec.s));
+  rec(11, wenc_host::launch_gemm(h->tm_a2, h->tm_wc2, B * T, d, 3 * d, h->bn_stem, wenc_host::kEpiGeluTable, h->cb2,
+                                 h->pos, x, h->err_dev, h->num_sms, rec.s, h->tf32, T));
+}
+
+// The blocks first .. first+count-1 and, if final_ln, the final LayerNorm: in -> out.
+void enqueue_blocks(wenc* h, const float* in, float* out, int B, int first, int count, bool final_ln, LaunchRec& rec) {
+  const wenc_config& c = h->cfg;
+  const cudaStream_t s = rec.s;
+  const int d = c.d_model, f = c.ffn_dim, T = c.seq_len, H = c.n_heads;
+  const int M = B * T;
+  const float* src = in;  // the residual stream entering the next block
+  for (int l = first; l < first + count && rec.e == cudaSuccess; ++l) {
+    const wenc::Layer& P = h->layers[l];
+    const bool last = (l == first + count - 1);
+    float* dst_final = (last && !final_ln) ? out : h->x;
+    if (h->tf32) {
+      // TF32: every GEMM operand is fp32 rounded to TF32 by its producer.
+      rec(0, wenc_host::launch_layernorm(src, P.ln1_w, P.ln1_b, h->xn, M, d, c.ln_eps, 2, s));
+      rec(1, wenc_host::launch_gemm(h->tm_xn, P.tm_wqkv, M, 3 * d, d, h->bn_qkv, WENC_EPI_BIAS_BF16, P.bqkv, nullptr,
+                                    h->qkv, h->err_dev, h->num_sms, s, true));
+      rec(2, wenc_host::launch_attention_tf32(h->tm_q, h->tm_kv, h->tm_kv, 0, d, 2 * d, static_cast<float*>(h->o), d,
+                                              B, T, H, h->err_dev, s));
+      rec(3, wenc_host::launch_gemm(h->tm_o, P.tm_wo, M, d, d, h->bn_o, WENC_EPI_BIAS_RESID_F32, P.bo, src, h->x,
+                                    h->err_dev, h->num_sms, s, true));
+      rec(0, wenc_host::launch_layernorm(h->x, P.ln2_w, P.ln2_b, h->xn, M, d, c.ln_eps, 2, s));
+      rec(4, wenc_host::launch_gemm(h->tm_xn, P.tm_w1, M, f, d, h->bn_1, WENC_EPI_BIAS_GELU_BF16, P.b1, nullptr, h->u,
+                                    h->err_dev, h->num_sms, s, true));
+      rec(5, wenc_host::launch_gemm(h->tm_u, P.tm_w2, M, d, f, h->bn_2, WENC_EPI_BIAS_RESID_F32, P.b2, h->x, dst_final,
+                                    h->err_dev, h->num_sms, s, true));
+      src = h->x;
+      continue;
+    }
+    uint16_t* o16 = static_cast<uint16_t*>(h->o);
+    rec(0, wenc_host::launch_layernorm(src, P.ln1_w, P.ln1_b, h->xn, M, d, c.ln_eps, 1, s));
+    rec(1, wenc_host::launch_gemm(h->tm_xn, P.tm_wqkv, M, 3 * d, d, h->bn_qkv, WENC_EPI_BIAS_BF16, P.bqkv, nullptr,
+                                  h->qkv, h->err_dev, h->num_sms, s));
+    rec(2, wenc_host::launch_attention_main(h->tm_q, h->tm_kv, h->tm_kv, 0, d, 2 * d, o16, d, B, T, H, h->err_dev, s,
+                                            h->attn_splits, h->part_o, h->part_ml));
+    if (wenc_host::attention_launches(T, h->attn_splits) == 2)
+      rec(8, wenc_host::launch_attention_combine(h->part_o, h->part_ml, o16, d, B, T, H, h->attn_splits, s));
+    rec(3, wenc_host::launch_gemm(h->tm_o, P.tm_wo, M, d, d, h->bn_o, WENC_EPI_BIAS_RESID_F32, P.bo, src, h->x,
+                                  h->err_dev, h->num_sms, s));
+    rec(0, wenc_host::launch_layernorm(h->x, P.ln2_w, P.ln2_b, h->xn, M, d, c.ln_eps, 1, s));
+    rec(4, wenc_host::launch_gemm(h->tm_xn, P.tm_w1, M, f, d, h->bn_1, WENC_EPI_BIAS_GELU_BF16, P.b1, nullptr, h->u,
+                                  h->err_dev, h->num_sms, s));
+    rec(5, wenc_host::launch_gemm(h->tm_u, P.tm_w2, M, d, f, h->bn_2, WENC_EPI_BIAS_RESID_F32, P.b2, h->x, dst_final,
+                                  h->err_dev, h->num_sms, s));
+    src = h->x;
+  }
+  if (rec.e == cudaSuccess) {
+    if (final_ln) {
+      rec(6, wenc_host::launch_layernorm(src, h->lnf_w, h->lnf_b, out, M, d, c.ln_eps, 0, s));
+    } else if (count == 0) {
+      rec(7, in == out ? cudaSuccess : cudaMemcpyAsync(out, in, size_t(M) * d * 4, cudaMemcpyDeviceToDevice, s));
+    }
+  }
 }
 
 }  // namespace
@@ -497,93 +618,119 @@ wenc_status wenc_forward_layers(wenc* h, const float* in, float* out, int B, int
   g_last_error.clear();
   if (!h) return fail(WENC_ERR_INVALID_ARG, "handle is NULL");
   const wenc_config& c = h->cfg;
-  if (!in || !out) return fail(WENC_ERR_INVALID_ARG, "hidden_in/hidden_out is NULL");
-  if (!aligned16(in) || !aligned16(out)) return fail(WENC_ERR_INVALID_ARG, "hidden buffers must be 16-byte aligned");
-  if (B < 1 || B > c.max_batch) return fail(WENC_ERR_INVALID_ARG, "B = %d outside 1..max_batch %d", B, c.max_batch);
   if (first < 0 || count < 0 || first + count > c.n_layers)
     return fail(WENC_ERR_INVALID_ARG, "layers %d..%d outside 0..%d", first, first + count - 1, c.n_layers - 1);
-  int dev = -1;
-  cudaGetDevice(&dev);
-  if (dev != h->device) return fail(WENC_ERR_INVALID_ARG, "current device %d is not the handle's device %d", dev, h->device);
-  if (*reinterpret_cast<volatile uint32_t*>(h->err_host) != 0)
-    return fail(WENC_ERR_DEVICE_TIMEOUT, "an earlier launch recorded device error word 0x%x",
-                *reinterpret_cast<volatile uint32_t*>(h->err_host));
-
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream_);
-  const int d = c.d_model, f = c.ffn_dim, T = c.seq_len, H = c.n_heads;
-  const int M = B * T;
-  const bool final_ln = apply_final_ln && c.final_ln;
-  const int n_launch = wenc_forward_launches(h, first, count, apply_final_ln);
-  std::vector<cudaEvent_t> ev;
-  ev.swap(h->events);
-  int* kinds = h->kinds;
-  h->kinds = nullptr;
-  if (!ev.empty() && static_cast<int>(ev.size()) < n_launch + 1)
-    return fail(WENC_ERR_INVALID_ARG, "launch events: need %d, got %zu", n_launch + 1, ev.size());
-
-  int li = 0;
-  cudaError_t e = cudaSuccess;
-  auto rec = [&](int kind, cudaError_t le) {
-    if (e == cudaSuccess) e = le;
-    if (kinds) kinds[li] = kind;
-    ++li;
-    if (!ev.empty() && e == cudaSuccess) e = cudaEventRecord(ev[li], s);
-  };
-  if (!ev.empty()) e = cudaEventRecord(ev[0], s);
-
-  const float* src = in;  // the residual stream entering the next block
-  for (int l = first; l < first + count && e == cudaSuccess; ++l) {
-    const wenc::Layer& P = h->layers[l];
-    const bool last = (l == first + count - 1);
-    float* dst_final = (last && !final_ln) ? out : h->x;
-    if (h->tf32) {
-      // TF32: every GEMM operand is fp32 rounded to TF32 by its producer.
-      rec(0, wenc_host::launch_layernorm(src, P.ln1_w, P.ln1_b, h->xn, M, d, c.ln_eps, 2, s));
-      rec(1, wenc_host::launch_gemm(h->tm_xn, P.tm_wqkv, M, 3 * d, d, h->bn_qkv, WENC_EPI_BIAS_BF16, P.bqkv, nullptr,
-                                    h->qkv, h->err_dev, h->num_sms, s, true));
-      rec(2, wenc_host::launch_attention_tf32(h->tm_q, h->tm_kv, h->tm_kv, 0, d, 2 * d, static_cast<float*>(h->o), d,
-                                              B, T, H, h->err_dev, s));
-      rec(3, wenc_host::launch_gemm(h->tm_o, P.tm_wo, M, d, d, h->bn_o, WENC_EPI_BIAS_RESID_F32, P.bo, src, h->x,
-                                    h->err_dev, h->num_sms, s, true));
-      rec(0, wenc_host::launch_layernorm(h->x, P.ln2_w, P.ln2_b, h->xn, M, d, c.ln_eps, 2, s));
-      rec(4, wenc_host::launch_gemm(h->tm_xn, P.tm_w1, M, f, d, h->bn_1, WENC_EPI_BIAS_GELU_BF16, P.b1, nullptr, h->u,
-                                    h->err_dev, h->num_sms, s, true));
-      rec(5, wenc_host::launch_gemm(h->tm_u, P.tm_w2, M, d, f, h->bn_2, WENC_EPI_BIAS_RESID_F32, P.b2, h->x, dst_final,
-                                    h->err_dev, h->num_sms, s, true));
-      src = h->x;
-      continue;
-    }
-    uint16_t* o16 = static_cast<uint16_t*>(h->o);
-    rec(0, wenc_host::launch_layernorm(src, P.ln1_w, P.ln1_b, h->xn, M, d, c.ln_eps, 1, s));
-    rec(1, wenc_host::launch_gemm(h->tm_xn, P.tm_wqkv, M, 3 * d, d, h->bn_qkv, WENC_EPI_BIAS_BF16, P.bqkv, nullptr,
-                                  h->qkv, h->err_dev, h->num_sms, s));
-    rec(2, wenc_host::launch_attention_main(h->tm_q, h->tm_kv, h->tm_kv, 0, d, 2 * d, o16, d, B, T, H, h->err_dev, s,
-                                            h->attn_splits, h->part_o, h->part_ml));
-    if (wenc_host::attention_launches(T, h->attn_splits) == 2)
-      rec(8, wenc_host::launch_attention_combine(h->part_o, h->part_ml, o16, d, B, T, H, h->attn_splits, s));
-    rec(3, wenc_host::launch_gemm(h->tm_o, P.tm_wo, M, d, d, h->bn_o, WENC_EPI_BIAS_RESID_F32, P.bo, src, h->x,
-                                  h->err_dev, h->num_sms, s));
-    rec(0, wenc_host::launch_layernorm(h->x, P.ln2_w, P.ln2_b, h->xn, M, d, c.ln_eps, 1, s));
-    rec(4, wenc_host::launch_gemm(h->tm_xn, P.tm_w1, M, f, d, h->bn_1, WENC_EPI_BIAS_GELU_BF16, P.b1, nullptr, h->u,
-                                  h->err_dev, h->num_sms, s));
-    rec(5, wenc_host::launch_gemm(h->tm_u, P.tm_w2, M, d, f, h->bn_2, WENC_EPI_BIAS_RESID_F32, P.b2, h->x, dst_final,
-                                  h->err_dev, h->num_sms, s));
-    src = h->x;
-  }
-  if (e == cudaSuccess) {
-    if (final_ln) {
-      rec(6, wenc_host::launch_layernorm(src, h->lnf_w, h->lnf_b, out, M, d, c.ln_eps, 0, s));
-    } else if (count == 0) {
-      rec(7, in == out ? cudaSuccess : cudaMemcpyAsync(out, in, size_t(M) * d * 4, cudaMemcpyDeviceToDevice, s));
-    }
-  }
-  if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+  LaunchRec rec;
+  wenc_status st = begin_call(h, in, out, B, wenc_forward_launches(h, first, count, apply_final_ln),
+                              reinterpret_cast<cudaStream_t>(stream_), &rec);
+  if (st != WENC_OK) return st;
+  enqueue_blocks(h, in, out, B, first, count, apply_final_ln && c.final_ln, rec);
+  if (rec.e != cudaSuccess) return cuda_fail(rec.e, "forward launch");
   return WENC_OK;
 }
 
 wenc_status wenc_forward(wenc* h, const float* in, float* out, int B, wenc_stream_t stream) {
   if (!h) return fail(WENC_ERR_INVALID_ARG, "handle is NULL");
   return wenc_forward_layers(h, in, out, B, 0, h->cfg.n_layers, 1, stream);
+}
+
+wenc_status wenc_set_stem(wenc* h, const wenc_stem_weights* w, wenc_stream_t stream_) {
+  g_last_error.clear();
+  if (!h) return fail(WENC_ERR_INVALID_ARG, "handle is NULL");
+  if (!w) return fail(WENC_ERR_INVALID_ARG, "stem weights are NULL");
+  const void* req[] = {w->conv1_w, w->conv1_b, w->conv2_w, w->conv2_b, w->positions};
+  for (const void* p : req) {
+    if (!p) return fail(WENC_ERR_INVALID_ARG, "a stem weight pointer is NULL");
+    if (!is_device_accessible(p)) return fail(WENC_ERR_INVALID_ARG, "a stem weight pointer is not device memory");
+  }
+  if (w->n_mels < 8 || w->n_mels > 1024 || w->n_mels % 8 != 0)
+    return fail(WENC_ERR_INVALID_ARG, "n_mels %d: a multiple of 8 in 8..1024", w->n_mels);
+  const wenc_config& c = h->cfg;
+  const int d = c.d_model, T = c.seq_len, nm = w->n_mels;
+  const size_t es = h->esz;
+  const int kp1 = (3 * nm + 63) / 64 * 64;  // conv1's K, padded to whole 64-element stages
+  const size_t rows1 = size_t(c.max_batch) * 2 * T, rows2 = size_t(c.max_batch) * T;
+  Arena ar;
+  const size_t o_wc1 = ar.take(size_t(d) * kp1 * es), o_wc2 = ar.take(size_t(d) * 3 * d * es);
+  const size_t o_cb1 = ar.take(size_t(d) * 4), o_cb2 = ar.take(size_t(d) * 4), o_pos = ar.take(size_t(T) * d * 4);
+  const size_t o_a1 = ar.take(rows1 * kp1 * es), o_h1 = ar.take(rows1 * d * es), o_a2 = ar.take(rows2 * 3 * d * es);
+  if (h->stem_arena) {
+    cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream_));
+    cudaFree(h->stem_arena);
+    h->stem_arena = nullptr;
+  }
+  h->has_stem = false;
+  cudaError_t e = cudaMalloc(&h->stem_arena, ar.used);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    h->stem_arena = nullptr;
+    return fail(WENC_ERR_OOM, "stem: cudaMalloc(%zu) failed", ar.used);
+  }
+  uint8_t* base = static_cast<uint8_t*>(h->stem_arena);
+  h->n_mels = nm;
+  h->kp1 = kp1;
+  h->bn_stem = wenc_host::gemm_pick_bn(d);
+  h->wc1 = base + o_wc1;
+  h->wc2 = base + o_wc2;
+  h->cb1 = reinterpret_cast<float*>(base + o_cb1);
+  h->cb2 = reinterpret_cast<float*>(base + o_cb2);
+  h->pos = reinterpret_cast<float*>(base + o_pos);
+  h->a1 = base + o_a1;
+  h->h1 = base + o_h1;
+  h->a2 = base + o_a2;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream_);
+  const bool wbf16 = c.weight_dtype == WENC_DTYPE_BF16;
+  e = wenc_host::launch_conv_weight(w->conv1_w, wbf16, h->wc1, h->tf32, d, nm, kp1, s);
+  if (e == cudaSuccess) e = wenc_host::launch_conv_weight(w->conv2_w, wbf16, h->wc2, h->tf32, d, d, 3 * d, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(h->cb1, w->conv1_b, size_t(d) * 4, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(h->cb2, w->conv2_b, size_t(d) * 4, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(h->pos, w->positions, size_t(T) * d * 4, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "packing the stem");
+  std::string why;
+  const uint32_t kbox = h->tf32 ? 32 : 64;
+  bool ok = true;
+  auto map2 = [&](CUtensorMap* m, const void* p, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+    ok = ok && (h->tf32 ? wenc_host::make_tmap_2d_f32(m, p, inner, outer, inner * 4, kbox, box_outer, &why)
+                        : wenc_host::make_tmap_2d_bf16(m, p, inner, outer, inner * 2, kbox, box_outer, &why));
+  };
+  map2(&h->tm_a1, h->a1, kp1, rows1, wenc_host::kGemmBM);
+  map2(&h->tm_wc1, h->wc1, kp1, d, h->bn_stem);
+  map2(&h->tm_a2, h->a2, 3 * d, rows2, wenc_host::kGemmBM);
+  map2(&h->tm_wc2, h->wc2, 3 * d, d, h->bn_stem);
+  if (!ok) return fail(WENC_ERR_CUDA, "%s", why.c_str());
+  h->has_stem = true;
+  return WENC_OK;
+}
+
+int wenc_encode_launches(const wenc* h) {
+  if (!h || !h->has_stem) return -1;
+  return 4 + wenc_forward_launches(h, 0, h->cfg.n_layers, 1);
+}
+
+wenc_status wenc_stem(wenc* h, const float* mel, float* out, int B, wenc_stream_t stream_) {
+  g_last_error.clear();
+  if (!h) return fail(WENC_ERR_INVALID_ARG, "handle is NULL");
+  if (!h->has_stem) return fail(WENC_ERR_INVALID_ARG, "no stem: call wenc_set_stem first");
+  LaunchRec rec;
+  wenc_status st = begin_call(h, mel, out, B, 4, reinterpret_cast<cudaStream_t>(stream_), &rec);
+  if (st != WENC_OK) return st;
+  enqueue_stem(h, mel, out, B, rec);
+  if (rec.e != cudaSuccess) return cuda_fail(rec.e, "stem launch");
+  return WENC_OK;
+}
+
+wenc_status wenc_encode(wenc* h, const float* mel, float* out, int B, wenc_stream_t stream_) {
+  g_last_error.clear();
+  if (!h) return fail(WENC_ERR_INVALID_ARG, "handle is NULL");
+  if (!h->has_stem) return fail(WENC_ERR_INVALID_ARG, "no stem: call wenc_set_stem first");
+  LaunchRec rec;
+  wenc_status st = begin_call(h, mel, out, B, wenc_encode_launches(h), reinterpret_cast<cudaStream_t>(stream_), &rec);
+  if (st != WENC_OK) return st;
+  enqueue_stem(h, mel, h->x, B, rec);  // the stem writes the residual stream the blocks start from
+  if (rec.e == cudaSuccess) enqueue_blocks(h, h->x, out, B, 0, h->cfg.n_layers, h->cfg.final_ln != 0, rec);
+  if (rec.e != cudaSuccess) return cuda_fail(rec.e, "encode launch");
+  return WENC_OK;
 }
 
 wenc_status wenc_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* out, int B, int T, int H,

@@ -7,6 +7,8 @@
 //   QKV:      bf16 out = A W^T + b             (b's K slot is zero)
 //   fc1:      bf16 out = GELU_erf(A W^T + b)
 //   out, fc2: f32  out = resid + (A W^T + b)   (the residual add, in place on x)
+//   conv2:    f32  out = GELU_erf(A W^T + b) + table[row % period]   (the stem's last
+//             convolution with its positional rows, turbospark-runtime encode_partial)
 // The TF32 form of the kernel takes fp32 A and W (already rounded to TF32 by their producers)
 // and runs kind::tf32 MMAs (128 x BN x 8); its QKV and fc1 outputs are fp32 rounded to TF32.
 //
@@ -80,19 +82,22 @@ __device__ __forceinline__ uint32_t stage_addr(uint32_t stage, int row, int gran
   return stage + row * 128 + ((granule ^ (row & 7)) << 4);
 }
 
-// Residual values this lane will need for one chunk (rows grow0 + 4i + lane/8).
+// Residual (or table) values this lane will need for one chunk (rows grow0 + 4i + lane/8).
+// With period > 0 output row r reads table row r % period.
 __device__ __forceinline__ void load_resid(float4 (&rr)[8], const float* resid, int grow0, int M, int N, int col,
-                                           int lane) {
+                                           int lane, int period) {
   const int sub = lane >> 3, cl = lane & 7;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int grow = grow0 + 4 * i + sub;
-    if (grow < M) rr[i] = *reinterpret_cast<const float4*>(resid + static_cast<size_t>(grow) * N + col + 4 * cl);
+    const int srow = period > 0 ? grow % period : grow;
+    if (grow < M) rr[i] = *reinterpret_cast<const float4*>(resid + static_cast<size_t>(srow) * N + col + 4 * cl);
   }
 }
 
-// EPI 0 = bias, 1 = bias + GELU, 2 = residual + bias (fp32 out). For EPI 0 and 1 the output
-// is bf16 (F32OUT false) or fp32 rounded to TF32 (F32OUT true: the operand of a TF32 GEMM).
+// EPI 0 = bias, 1 = bias + GELU, 2 = residual + bias (fp32 out), 3 = GELU(bias) + table row
+// (fp32 out). For EPI 0 and 1 the output is bf16 (F32OUT false) or fp32 rounded to TF32
+// (F32OUT true: the operand of a TF32 GEMM).
 template <int EPI, bool F32OUT>
 __device__ __forceinline__ void epilogue_chunk(const uint32_t (&acc)[32], uint32_t stage, int lane, int grow0, int M,
                                                int N, int col, const float* __restrict__ bias,
@@ -114,6 +119,10 @@ __device__ __forceinline__ void epilogue_chunk(const uint32_t (&acc)[32], uint32
       if constexpr (EPI == 2) {
         v = make_float4(rr[i].x + v.x, rr[i].y + v.y, rr[i].z + v.z, rr[i].w + v.w);
         *reinterpret_cast<float4*>(static_cast<float*>(out) + off) = v;
+      } else if constexpr (EPI == 3) {
+        v = make_float4(gelu_erf(v.x) + rr[i].x, gelu_erf(v.y) + rr[i].y, gelu_erf(v.z) + rr[i].z,
+                        gelu_erf(v.w) + rr[i].w);
+        *reinterpret_cast<float4*>(static_cast<float*>(out) + off) = v;
       } else {
         if constexpr (EPI == 1) {
           v.x = gelu_erf(v.x); v.y = gelu_erf(v.y); v.z = gelu_erf(v.z); v.w = gelu_erf(v.w);
@@ -133,7 +142,8 @@ __device__ __forceinline__ void epilogue_chunk(const uint32_t (&acc)[32], uint32
 template <int BN, int EPI, bool TF32>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, int M, int N,
-                   int K, const float* __restrict__ bias, const float* resid, void* out, uint32_t* err) {
+                   int K, const float* __restrict__ bias, const float* resid, void* out, uint32_t* err,
+                   int row_period) {
   using C = GemmCfg<BN>;
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -260,10 +270,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto row0_of = [&](int t) { return (t / n_tiles) * BM + quad * 32; };
     auto col_of = [&](int t) { return (t % n_tiles) * BN + col_half * (BN / 2); };
     float4 rb[2][8];
-    if constexpr (EPI == 2) {
+    constexpr bool kRowInput = (EPI == 2 || EPI == 3);  // residual rows or table rows
+    if constexpr (kRowInput) {
       if (blockIdx.x < num_tiles) {
-        load_resid(rb[0], resid, row0_of(blockIdx.x), M, N, col_of(blockIdx.x), lane);
-        if (CH > 1) load_resid(rb[1], resid, row0_of(blockIdx.x), M, N, col_of(blockIdx.x) + 32, lane);
+        load_resid(rb[0], resid, row0_of(blockIdx.x), M, N, col_of(blockIdx.x), lane, row_period);
+        if (CH > 1) load_resid(rb[1], resid, row0_of(blockIdx.x), M, N, col_of(blockIdx.x) + 32, lane, row_period);
       }
     }
     int local = 0;
@@ -287,11 +298,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive(tempty_bar(acc));
         }
         epilogue_chunk<EPI, TF32>(r, stage, lane, grow0, M, N, c0 + c * 32, bias, rb[c & 1], out);
-        if constexpr (EPI == 2) {
+        if constexpr (kRowInput) {
           if (c + 2 < CH) {
-            load_resid(rb[c & 1], resid, grow0, M, N, c0 + (c + 2) * 32, lane);
+            load_resid(rb[c & 1], resid, grow0, M, N, c0 + (c + 2) * 32, lane, row_period);
           } else if (next < num_tiles) {
-            load_resid(rb[c & 1], resid, row0_of(next), M, N, col_of(next) + (c + 2 - CH) * 32, lane);
+            load_resid(rb[c & 1], resid, row0_of(next), M, N, col_of(next) + (c + 2 - CH) * 32, lane, row_period);
           }
         }
       }
@@ -308,7 +319,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int BN, int EPI, bool TF32>
 cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmW, int M, int N, int K, const float* bias,
-                       const float* resid, void* out, uint32_t* err, int num_sms, cudaStream_t stream) {
+                       const float* resid, void* out, uint32_t* err, int num_sms, cudaStream_t stream,
+                       int row_period) {
   using C = GemmCfg<BN>;
   auto kern = gemm_tc_kernel<BN, EPI, TF32>;
   static int configured_device = -1;  // attribute is per device; cheap to repeat
@@ -322,7 +334,7 @@ cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmW, int M, in
   const int tiles = ((M + BM - 1) / BM) * (N / BN);
   const int grid = tiles < num_sms ? tiles : num_sms;
   return wenc_host::launch_pdl(kern, dim3(grid), dim3(kThreads), C::SMEM, stream, tmA, tmW, M, N, K, bias, resid, out,
-                               err);
+                               err, row_period);
 }
 
 }  // namespace
@@ -337,23 +349,28 @@ int gemm_pick_bn(int N) {
 
 cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmW, int M, int N, int K, int bn, int epilogue,
                         const float* bias, const float* resid, void* out, uint32_t* err, int num_sms,
-                        cudaStream_t stream, bool tf32) {
+                        cudaStream_t stream, bool tf32, int row_period) {
   if (M <= 0) return cudaSuccess;
+  if (epilogue == 3 && row_period <= 0) return cudaErrorInvalidValue;
 #define WENC_GEMM_CASE(BNV, EPIV, TF) \
   if (bn == BNV && epilogue == EPIV && tf32 == TF)                                        \
-    return launch_one<BNV, EPIV, TF>(tmA, tmW, M, N, K, bias, resid, out, err, num_sms, stream);
+    return launch_one<BNV, EPIV, TF>(tmA, tmW, M, N, K, bias, resid, out, err, num_sms, stream, row_period);
   WENC_GEMM_CASE(256, 0, false)
   WENC_GEMM_CASE(256, 1, false)
   WENC_GEMM_CASE(256, 2, false)
   WENC_GEMM_CASE(128, 0, false)
   WENC_GEMM_CASE(128, 1, false)
   WENC_GEMM_CASE(128, 2, false)
+  WENC_GEMM_CASE(256, 3, false)
+  WENC_GEMM_CASE(128, 3, false)
   WENC_GEMM_CASE(256, 0, true)
   WENC_GEMM_CASE(256, 1, true)
   WENC_GEMM_CASE(256, 2, true)
   WENC_GEMM_CASE(128, 0, true)
   WENC_GEMM_CASE(128, 1, true)
   WENC_GEMM_CASE(128, 2, true)
+  WENC_GEMM_CASE(256, 3, true)
+  WENC_GEMM_CASE(128, 3, true)
 #undef WENC_GEMM_CASE
   return cudaErrorInvalidValue;
 }

@@ -61,9 +61,12 @@ constexpr int kGemmBK = 64;
 // tf32 = false: bf16 A and W (maps with box 64 x rows), epilogues 0, 1, 2.
 // tf32 = true: fp32 A and W read as TF32 (maps with box 32 x rows); epilogues 0 and 1 write
 // fp32 rounded to TF32 instead of bf16. K must be a multiple of 64 (bf16) or 32 (TF32).
+// Epilogue 3 (internal, the stem's conv2): out fp32 = GELU_erf(A W^T + bias) + resid[row % row_period]
+// with resid a [row_period, N] fp32 table (row_period > 0).
+constexpr int kEpiGeluTable = 3;
 cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmW, int M, int N, int K, int bn, int epilogue,
                         const float* bias, const float* resid, void* out, uint32_t* err, int num_sms,
-                        cudaStream_t stream, bool tf32 = false);
+                        cudaStream_t stream, bool tf32 = false, int row_period = 0);
 
 // ---------------------------------------------------------------- attention (tcgen05)
 // Q/K/V tiles are read through 3-D maps [B][T][row] (box 64 x 128 elements for all three);
@@ -98,6 +101,18 @@ constexpr int kAttnTf32BKV = 64;
 cudaError_t launch_attention_tf32(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, int q_col0,
                                   int k_col0, int v_col0, float* out, int out_stride, int B, int T, int H,
                                   uint32_t* err, cudaStream_t stream);
+
+// ---------------------------------------------------------------- convolutional stem
+// Unfold for a kernel-3, padding-1 convolution over time: x [B, t_in, C] (fp32, or the operand
+// format: bf16 / TF32-rounded fp32) -> A [B * t_out, k_pad] in the operand format with
+// A[b*t_out + t, j*C + i] = x[b, stride*t + j - 1, i] (0 outside the window) and zeros in
+// columns 3C .. k_pad-1. C % 8 == 0, k_pad % 8 == 0, k_pad >= 3C.
+cudaError_t launch_unfold3(const void* x, bool x_f32, void* a, bool a_tf32, int B, int t_in, int C, int stride,
+                           int k_pad, cudaStream_t stream);
+// Weight in unfold order: w [C_out, C_in, 3] (fp32 or bf16) -> wp [C_out, k_pad] in the operand
+// format with wp[o, j*C_in + i] = w[o, i, j], zeros in columns 3*C_in .. k_pad-1.
+cudaError_t launch_conv_weight(const void* w, bool w_bf16, void* wp, bool wp_tf32, int c_out, int c_in, int k_pad,
+                               cudaStream_t stream);
 
 // ---------------------------------------------------------------- weight packing
 cudaError_t launch_f32_to_bf16(const float* src, uint16_t* dst, size_t n, cudaStream_t stream);

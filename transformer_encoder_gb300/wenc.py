@@ -24,13 +24,14 @@ LN_OUT_F32, LN_OUT_BF16, LN_OUT_TF32 = 0, 1, 2
 PREC_BF16, PREC_TF32 = 0, 1
 _STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "OOM", 4: "CUDA", 5: "DEVICE_TIMEOUT"}
 LAUNCH_KINDS = {0: "layernorm", 1: "gemm_qkv", 2: "attention", 3: "gemm_out", 4: "gemm_fc1", 5: "gemm_fc2",
-                6: "layernorm_final", 7: "copy", 8: "attention_combine"}
+                6: "layernorm_final", 7: "copy", 8: "attention_combine", 9: "stem_unfold", 10: "gemm_conv1",
+                11: "gemm_conv2"}
 
 EXPORTED_SYMBOLS = (
     "wenc_create", "wenc_forward", "wenc_forward_layers", "wenc_forward_launches", "wenc_set_launch_events",
     "wenc_attention", "wenc_layernorm", "wenc_linear", "wenc_sync_status", "wenc_destroy", "wenc_last_error",
     "wenc_version", "wenc_selftest_wait_timeout", "wenc_attention_static", "wenc_attention_static_capacity",
-    "wenc_linear_tf32", "wenc_attention_tf32",
+    "wenc_linear_tf32", "wenc_attention_tf32", "wenc_set_stem", "wenc_stem", "wenc_encode", "wenc_encode_launches",
 )
 
 
@@ -54,6 +55,13 @@ class LayerWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in _LW_FIELDS]
 
 
+STEM_KEYS = ("conv1_w", "conv1_b", "conv2_w", "conv2_b", "positions")
+
+
+class StemWeights(ctypes.Structure):
+    _fields_ = [("n_mels", ctypes.c_int)] + [(n, ctypes.c_void_p) for n in STEM_KEYS]
+
+
 _lib = None
 
 
@@ -74,6 +82,10 @@ def lib() -> ctypes.CDLL:
         L.wenc_layernorm.argtypes = [vp, vp, vp, vp, i, i, f, i, vp]
         L.wenc_linear.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, vp]
         L.wenc_linear_tf32.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, vp]
+        L.wenc_set_stem.argtypes = [vp, ctypes.POINTER(StemWeights), vp]
+        L.wenc_stem.argtypes = [vp, vp, vp, i, vp]
+        L.wenc_encode.argtypes = [vp, vp, vp, i, vp]
+        L.wenc_encode_launches.argtypes = [vp]
         L.wenc_attention_tf32.argtypes = [vp, vp, vp, vp, i, i, i, i, vp]
         L.wenc_sync_status.argtypes = [vp]
         L.wenc_selftest_wait_timeout.argtypes = [vp]
@@ -87,7 +99,8 @@ def lib() -> ctypes.CDLL:
         L.wenc_version.restype = ctypes.c_char_p
         for name in ("wenc_create", "wenc_forward", "wenc_forward_layers", "wenc_set_launch_events", "wenc_attention",
                      "wenc_layernorm", "wenc_linear", "wenc_sync_status", "wenc_forward_launches",
-                     "wenc_selftest_wait_timeout", "wenc_linear_tf32", "wenc_attention_tf32"):
+                     "wenc_selftest_wait_timeout", "wenc_linear_tf32", "wenc_attention_tf32", "wenc_set_stem",
+                     "wenc_stem", "wenc_encode", "wenc_encode_launches"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -181,6 +194,43 @@ class Encoder:
         B = x.shape[0]
         _check(lib().wenc_forward_layers(self._h, _ptr(x), _ptr(out), B, first, count, int(final_ln), _stream(stream)))
         return out
+
+    def set_stem(self, stem: dict, stream=None):
+        """Attach the convolutional stem: ``stem`` has the keys of ``STEM_KEYS`` as CUDA tensors
+        (conv weights [d, C_in, 3] in the layers' matrix dtype, biases [d] and positions
+        [seq_len, d] float32); n_mels is read from conv1_w."""
+        import torch
+        mdtype = torch.bfloat16 if self.cfg.weight_dtype == 1 else torch.float32
+        _require(stem["conv1_w"], mdtype, "conv1_w")
+        _require(stem["conv2_w"], mdtype, "conv2_w")
+        for k in ("conv1_b", "conv2_b", "positions"):
+            _require(stem[k], torch.float32, k)
+        self.n_mels = int(stem["conv1_w"].shape[1])
+        w = StemWeights(self.n_mels, *[stem[k].data_ptr() for k in STEM_KEYS])
+        _check(lib().wenc_set_stem(self._h, ctypes.byref(w), _stream(stream)))
+
+    def stem(self, mel, out=None, stream=None):
+        """hidden [B, seq_len, d] = stem(mel), mel float32 CUDA [B, 2*seq_len, n_mels]."""
+        import torch
+        _require(mel, torch.float32, "mel")
+        if out is None:
+            out = torch.empty((mel.shape[0], self.seq_len, self.d_model), dtype=torch.float32, device=mel.device)
+        _require(out, torch.float32, "out")
+        _check(lib().wenc_stem(self._h, _ptr(mel), _ptr(out), mel.shape[0], _stream(stream)))
+        return out
+
+    def encode(self, mel, out=None, stream=None):
+        """The whole encoder from log-mel frames: stem, blocks and the final LayerNorm."""
+        import torch
+        _require(mel, torch.float32, "mel")
+        if out is None:
+            out = torch.empty((mel.shape[0], self.seq_len, self.d_model), dtype=torch.float32, device=mel.device)
+        _require(out, torch.float32, "out")
+        _check(lib().wenc_encode(self._h, _ptr(mel), _ptr(out), mel.shape[0], _stream(stream)))
+        return out
+
+    def encode_launches(self) -> int:
+        return lib().wenc_encode_launches(self._h)
 
     def launches(self, first: int = 0, count: int | None = None, final_ln: bool = True) -> int:
         count = self.n_layers - first if count is None else count
