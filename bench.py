@@ -12,6 +12,9 @@ same C-ABI call with the input copied from pinned host memory and the output cop
 inside the timed region. Multi-GPU runs are independent replicas (windows are independent;
 there is no collective on the data path): value = all ranks' windows / the slowest rank's time.
 
+`--stem` makes a step the whole encoder from log-mel frames (wenc_encode: the convolutional stem,
+the blocks and the final LayerNorm) with the input [B, 3000, n_mels] on the device.
+
 `--precision tf32` runs the same step with TF32 tensor-core operands and fp32 activations; its
 roofline peak is the measured bf16 peak times the nominal TF32/BF16 ratio (1.1 / 2.25 PFLOP/s).
 
@@ -200,6 +203,26 @@ def time_oracle_block(w, seconds: float, steps: int | None = None):
     return times
 
 
+def time_oracle_stem(w, steps: int):
+    """Time the f64 oracle's convolutional stem on one window; returns the per-run seconds."""
+    import oracle
+    import synth
+    p = synth.make_stem(w)
+    mel = synth.make_mel(w, batch=1)[0]
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        oracle.conv_stem(mel, p["conv1_w"], p["conv1_b"], p["conv2_w"], p["conv2_b"], p["positions"])
+        times.append(time.perf_counter() - t0)
+    return times
+
+
+def stem_flops(w) -> float:
+    """Dense FLOPs of the stem per call: conv1 (2T x d x 3 n_mels) and conv2 (T x d x 3d)."""
+    d, T = w.d_model, w.seq_len
+    return 2.0 * w.batch * (2 * T * d * 3 * w.n_mels + T * d * 3 * d)
+
+
 def host_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -207,13 +230,16 @@ def host_cores():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(w, seconds: float):
+def cpu_baseline(w, seconds: float, with_stem: bool = False):
     times = time_oracle_block(w, seconds)
     t_block = statistics.median(times)
-    win_s = 1.0 / (t_block * w.n_layers)
+    t_stem = statistics.median(time_oracle_stem(w, 3)) if with_stem else 0.0
+    win_s = 1.0 / (t_block * w.n_layers + t_stem)
+    stem_note = f" + the stem ({t_stem:.3f} s, median of 3)" if with_stem else ""
     return {"value": win_s, "unit": "windows/s", "cores": host_cores(), "kind": "oracle",
             "sample": (f"f64 numpy oracle, one block of one {w.seq_len}-frame window at {w.name} dims, "
-                       f"median of {len(times)} runs ({t_block:.3f} s/block), extrapolated x{w.n_layers} blocks"),
+                       f"median of {len(times)} runs ({t_block:.3f} s/block), extrapolated x{w.n_layers} blocks"
+                       + stem_note),
             "seconds_per_block": t_block}
 
 
@@ -279,15 +305,24 @@ def run_wenc(args, w):
     tf32 = args.precision == "tf32"
     del dev_layers
     torch.cuda.empty_cache()
-    x_host = torch.from_numpy(synth.make_input(w, rng)).pin_memory()
+    if args.stem:
+        stem = synth.make_stem(w)
+        enc.set_stem({k: (torch.from_numpy(v).to(torch.bfloat16) if k in ("conv1_w", "conv2_w") and w.bf16_weights
+                          else torch.from_numpy(v)).cuda() for k, v in stem.items()})
+        x_host = torch.from_numpy(synth.make_mel(w)).pin_memory()
+        step = enc.encode
+        n_launch = enc.encode_launches()
+    else:
+        x_host = torch.from_numpy(synth.make_input(w, rng)).pin_memory()
+        step = enc.forward
+        n_launch = enc.launches()
     x = x_host.cuda()
-    out = torch.empty_like(x)
-    out_host = torch.empty_like(x_host).pin_memory()
+    out = torch.empty((w.batch, w.seq_len, w.d_model), dtype=torch.float32, device="cuda")
+    out_host = torch.empty(tuple(out.shape), dtype=torch.float32).pin_memory()
     stream = torch.cuda.current_stream()
 
-    n_launch = enc.launches()
     for _ in range(args.warmup):
-        enc.forward(x, out)
+        step(x, out)
     torch.cuda.synchronize()
     enc.sync_status()
 
@@ -308,7 +343,7 @@ def run_wenc(args, w):
     t_start.record(stream)
     for k in range(args.steps):
         ks = enc.set_launch_events(ev[k])
-        enc.forward(x, out)
+        step(x, out)
         if kinds is None:
             kinds = ks
     t_stop.record(stream)
@@ -330,7 +365,7 @@ def run_wenc(args, w):
     # ---- e2e through the same call with host buffers
     for _ in range(2):
         x.copy_(x_host, non_blocking=True)
-        enc.forward(x, out)
+        step(x, out)
         out_host.copy_(out, non_blocking=True)
     torch.cuda.synchronize()
     barrier()
@@ -339,7 +374,7 @@ def run_wenc(args, w):
     e_start.record(stream)
     for _ in range(args.steps):
         x.copy_(x_host, non_blocking=True)
-        enc.forward(x, out)
+        step(x, out)
         out_host.copy_(out, non_blocking=True)
     e_stop.record(stream)
     torch.cuda.synchronize()
@@ -351,7 +386,7 @@ def run_wenc(args, w):
     ms_step = ms_total / args.steps
     windows = w.batch * world
     value = job_throughput(w.batch, world, args.steps, ms_total)
-    flops_step = w.flops()
+    flops_step = w.flops() + (stem_flops(w) if args.stem else 0.0)
     tflops = flops_step * world / (ms_step / 1e3) / 1e12
 
     # ---- roofline of the dominant kernel (the tcgen05 GEMM: four launches per block)
@@ -360,6 +395,12 @@ def run_wenc(args, w):
                   "gemm_fc1": 2.0 * M * f * d, "gemm_fc2": 2.0 * M * d * f}
     attn_flops = 4.0 * w.batch * H * T * T * w.head_dim
     ln_bytes = (8.0 if tf32 else 6.0) * M * d  # fp32 read + bf16 or fp32 write
+    es = 4 if tf32 else 2
+    kp1 = (3 * w.n_mels + 63) // 64 * 64
+    stem_gemm_flops = {"gemm_conv1": 2.0 * w.batch * 2 * T * d * 3 * w.n_mels,
+                       "gemm_conv2": 2.0 * w.batch * T * d * 3 * d}
+    # both unfold launches of a step: read the signal, write the unfolded rows
+    unfold_bytes = (w.batch * 2 * T * (w.n_mels * 4 + kp1 * es)) + (w.batch * (2 * T * d * es + T * 3 * d * es))
     kern = {}
     for name, (ms, n) in per_kind.items():
         avg = ms / n
@@ -367,6 +408,10 @@ def run_wenc(args, w):
             kern[name] = {"launches": n, "avg_us": 1e3 * avg, "tflops": gemm_flops[name] / (avg / 1e3) / 1e12}
         elif name == "attention":
             kern[name] = {"launches": n, "avg_us": 1e3 * avg, "tflops": attn_flops / (avg / 1e3) / 1e12}
+        elif name in stem_gemm_flops:
+            kern[name] = {"launches": n, "avg_us": 1e3 * avg, "tflops": stem_gemm_flops[name] / (avg / 1e3) / 1e12}
+        elif name == "stem_unfold":
+            kern[name] = {"launches": n, "avg_us": 1e3 * avg, "gbs": unfold_bytes * args.steps / (ms / 1e3) / 1e9}
         elif name in ("layernorm", "layernorm_final"):
             b = ln_bytes if name == "layernorm" else 8.0 * M * d
             kern[name] = {"launches": n, "avg_us": 1e3 * avg, "gbs": b / (avg / 1e3) / 1e9}
@@ -399,7 +444,9 @@ def run_wenc(args, w):
         "metric": METRIC, "value": value, "unit": "windows/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "tf32" if tf32 else "bf16", "data": "synthetic",
-        "config": {"workload": workload_desc(w), "windows_per_step": w.batch, "seq_len": T,
+        "config": {"workload": workload_desc(w) + (f", from {2 * T} log-mel frames x {w.n_mels} through the "
+                                                   "convolutional stem" if args.stem else ""),
+                   "windows_per_step": w.batch, "seq_len": T,
                    "l2": "no flush: each step streams 1.26 GB of weights and >400 MB of activations, above the 126 MB L2"
                    if w.name == "large_stack" else "no flush",
                    "parallelism": f"replicas x{world}", "precision": args.precision},
@@ -415,7 +462,7 @@ def run_wenc(args, w):
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, with_stem=args.stem)
     if rank == 0:
         print(json.dumps(line), flush=True)
     enc.close()
@@ -434,6 +481,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="large_stack")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle's CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--stem", action="store_true",
+                    help="time the whole encoder from log-mel frames (convolutional stem + blocks)")
     ap.add_argument("--precision", choices=("bf16", "tf32"), default="bf16",
                     help="tensor-core operand precision of the timed path")
     args = ap.parse_args(argv)

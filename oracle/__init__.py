@@ -21,7 +21,9 @@ beyond what the definition states. Sources, by page and section:
 
 ``oracle.stem`` adds the convolutional stem in front of the blocks (conv1 and conv2
 with exact-erf GELU, then the positional rows), from turbospark-runtime
-``encode_partial`` and oxinfer ``WhisperModel::encode``.
+``encode_partial`` and oxinfer ``WhisperModel::encode``. ``oracle.cross`` adds the
+decoder's cross-attention K/V precompute over the encoder output (inferencelayer's
+cross K/V precompute, turbospark-runtime ``build_cross_caches``).
 
 Parity pins live in ``tests/test_oracle_pins.py``: hand-worked cases under
 ``tests/golden/``, closed forms, invariants and a cross-check against
@@ -32,3 +34,4 @@ from .encoder import (  # noqa: F401
     encoder_block, encoder_stack, block_rows, LN_EPS,
 )
 from .stem import conv1d, conv_stem  # noqa: F401
+from .cross import cross_kv  # noqa: F401

@@ -17,6 +17,7 @@ import numpy as np
 
 import oracle.encoder as E
 import oracle.stem as S
+import oracle.cross as X
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
@@ -309,6 +310,45 @@ def pin_conv_stem_torch():
         h = gelu(c1(torch.from_numpy(mel).transpose(1, 2)))
         ref = (gelu(c2(h)).transpose(1, 2) + torch.from_numpy(pos[:n])).numpy()
     _close(S.conv_stem(mel, w1, b1, w2, b2, pos), ref, rtol=1e-12, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------- cross K/V
+def pin_cross_kv_hand():
+    g = _golden("cross_kv_hand.json")
+    _close(X.cross_kv(g["enc_out"], g["wk"], g["wv"], g["bv"]), g["kv"], rtol=1e-14, atol=1e-15)
+
+
+def pin_cross_kv_closed_forms():
+    # A zero encoder output gives K = 0 (no K bias) and V = bv in every row; identity weights
+    # give K = enc_out and V = enc_out + bv.
+    rng = np.random.default_rng(14)
+    L, T, d = 3, 5, 4
+    wk = rng.standard_normal((L, d, d))
+    wv = rng.standard_normal((L, d, d))
+    bv = rng.standard_normal((L, d))
+    kv = X.cross_kv(np.zeros((T, d)), wk, wv, bv)
+    assert kv.shape == (2 * L, T, d)
+    _close(kv[0::2], np.zeros((L, T, d)))
+    _close(kv[1::2], np.broadcast_to(bv[:, None, :], (L, T, d)))
+    x = rng.standard_normal((2, T, d))
+    eye = np.broadcast_to(np.eye(d), (L, d, d))
+    kv = X.cross_kv(x, eye, eye, bv)
+    for l in range(L):
+        _close(kv[2 * l], x)
+        _close(kv[2 * l + 1], x + bv[l])
+
+
+def pin_cross_kv_torch():
+    import torch
+    rng = np.random.default_rng(15)
+    L, T, d = 2, 7, 6
+    x = rng.standard_normal((T, d))
+    wk, wv, bv = rng.standard_normal((L, d, d)), rng.standard_normal((L, d, d)), rng.standard_normal((L, d))
+    kv = X.cross_kv(x, wk, wv, bv)
+    tx = torch.from_numpy(x)
+    for l in range(L):
+        _close(kv[2 * l], torch.nn.functional.linear(tx, torch.from_numpy(wk[l])).numpy())
+        _close(kv[2 * l + 1], torch.nn.functional.linear(tx, torch.from_numpy(wv[l]), torch.from_numpy(bv[l])).numpy())
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -9,6 +9,7 @@ import pytest
 
 import oracle.encoder as E
 import oracle.stem as S
+import oracle.cross as X
 import oracle_pins as P
 
 
@@ -133,6 +134,17 @@ def _stem_variant(kind):
 
 _CONV = S.conv1d
 
+
+def _cross_variant(kind):
+    def cross(enc_out, wk, wv, bv):
+        planes = []
+        for k_w, v_w, v_b in zip(wk, wv, bv):
+            k = E.linear(enc_out, k_w, v_b if kind == "k_gets_v_bias" else None)
+            v = E.linear(enc_out, v_w, v_b)
+            planes += [v, k] if kind == "kv_swapped" else [k, v]
+        return np.stack(planes)
+    return cross
+
 MUTATIONS = {
     "ln_unbiased_variance": ("layer_norm", _ln_unbiased),
     "ln_missing_eps": ("layer_norm", _ln_no_eps),
@@ -159,6 +171,8 @@ MUTATIONS = {
     "stem_no_positions": ("S.conv_stem", _stem_variant("no_positions")),
     "stem_gelu_after_positions": ("S.conv_stem", _stem_variant("gelu_after_positions")),
     "stem_conv1_strided": ("S.conv_stem", _stem_variant("conv1_strided")),
+    "cross_k_gets_v_bias": ("X.cross_kv", _cross_variant("k_gets_v_bias")),
+    "cross_kv_planes_swapped": ("X.cross_kv", _cross_variant("kv_swapped")),
 }
 
 
@@ -168,6 +182,8 @@ def test_mutation_is_caught(name, monkeypatch):
     module = E
     if attr.startswith("S."):
         module, attr = S, attr[2:]
+    elif attr.startswith("X."):
+        module, attr = X, attr[2:]
     monkeypatch.setattr(module, attr, fn)
     caught = []
     for pin in P.ALL_PINS:

@@ -26,39 +26,44 @@ __device__ __forceinline__ void load8(const void* x, bool x_f32, size_t off, flo
   }
 }
 
-// One thread per 8 consecutive elements of an unfolded row.
+// One warp per unfolded row (window b, output position t): the row's source frames are found
+// once, and the lanes walk its 8-element chunks (chunk c: tap c / (C/8), channels 8 (c % (C/8))).
 template <bool X_F32, bool A_TF32>
 __global__ void __launch_bounds__(256) unfold3_kernel(const void* __restrict__ x, void* __restrict__ a, int t_in,
-                                                      int t_out, int C, int stride, int k_pad, long long total) {
+                                                      int t_out, int C, int stride, int k_pad, int rows) {
   wenc_dev::pdl_trigger();
   wenc_dev::pdl_wait();  // x from the previous kernel is complete from here on
+  const int lane = threadIdx.x & 31;
+  const int warps = gridDim.x * (blockDim.x >> 5);
   const int cpr = k_pad / 8;  // 8-element chunks per unfolded row
-  for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
-       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long row = idx / cpr;
-    const int col = static_cast<int>(idx % cpr) * 8;
-    const long long b = row / t_out;
-    const int t = static_cast<int>(row % t_out);
-    float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    uint4 raw = make_uint4(0u, 0u, 0u, 0u);  // bf16 input passed through unchanged
-    if (col < 3 * C) {
-      const int j = col / C, i = col % C;  // C % 8 == 0: a chunk never straddles two taps
-      const int src = stride * t + j - 1;
-      if (src >= 0 && src < t_in) load8(x, X_F32, (static_cast<size_t>(b) * t_in + src) * C + i, v, raw);
-    }
-    const size_t off = static_cast<size_t>(row) * k_pad + col;
-    if constexpr (A_TF32) {
-      float* dst = static_cast<float*>(a) + off;
-      *reinterpret_cast<float4*>(dst) = make_float4(wenc_dev::round_tf32(v[0]), wenc_dev::round_tf32(v[1]),
-                                                    wenc_dev::round_tf32(v[2]), wenc_dev::round_tf32(v[3]));
-      *reinterpret_cast<float4*>(dst + 4) = make_float4(wenc_dev::round_tf32(v[4]), wenc_dev::round_tf32(v[5]),
-                                                        wenc_dev::round_tf32(v[6]), wenc_dev::round_tf32(v[7]));
-    } else if constexpr (X_F32) {
-      *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a) + off) =
-          make_uint4(wenc_dev::pack_bf16x2(v[0], v[1]), wenc_dev::pack_bf16x2(v[2], v[3]),
-                     wenc_dev::pack_bf16x2(v[4], v[5]), wenc_dev::pack_bf16x2(v[6], v[7]));
-    } else {
-      *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a) + off) = raw;
+  const int cpt = C / 8;      // chunks per tap
+  for (int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows; row += warps) {
+    const int b = row / t_out;
+    const int t = row - b * t_out;
+    const size_t row_off = static_cast<size_t>(row) * k_pad;
+    for (int c = lane; c < cpr; c += 32) {
+      float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      uint4 raw = make_uint4(0u, 0u, 0u, 0u);  // bf16 input passed through unchanged
+      if (c < 3 * cpt) {
+        const int j = c / cpt;
+        const int i = (c - j * cpt) * 8;
+        const int src = stride * t + j - 1;
+        if (src >= 0 && src < t_in) load8(x, X_F32, (static_cast<size_t>(b) * t_in + src) * C + i, v, raw);
+      }
+      const size_t off = row_off + static_cast<size_t>(c) * 8;
+      if constexpr (A_TF32) {
+        float* dst = static_cast<float*>(a) + off;
+        *reinterpret_cast<float4*>(dst) = make_float4(wenc_dev::round_tf32(v[0]), wenc_dev::round_tf32(v[1]),
+                                                      wenc_dev::round_tf32(v[2]), wenc_dev::round_tf32(v[3]));
+        *reinterpret_cast<float4*>(dst + 4) = make_float4(wenc_dev::round_tf32(v[4]), wenc_dev::round_tf32(v[5]),
+                                                          wenc_dev::round_tf32(v[6]), wenc_dev::round_tf32(v[7]));
+      } else if constexpr (X_F32) {
+        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a) + off) =
+            make_uint4(wenc_dev::pack_bf16x2(v[0], v[1]), wenc_dev::pack_bf16x2(v[2], v[3]),
+                       wenc_dev::pack_bf16x2(v[4], v[5]), wenc_dev::pack_bf16x2(v[6], v[7]));
+      } else {
+        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a) + off) = raw;
+      }
     }
   }
 }
@@ -96,15 +101,17 @@ cudaError_t launch_unfold3(const void* x, bool x_f32, void* a, bool a_tf32, int 
   if (C % 8 != 0 || k_pad % 8 != 0 || k_pad < 3 * C || (stride != 1 && stride != 2)) return cudaErrorInvalidValue;
   if (!x_f32 && a_tf32) return cudaErrorInvalidValue;  // bf16 input only feeds a bf16 GEMM
   const int t_out = (t_in + 2 - 3) / stride + 1;
-  const long long total = static_cast<long long>(B) * t_out * (k_pad / 8);
-  if (total <= 0) return cudaSuccess;
-  const long long want = (total + 255) / 256;
-  const dim3 grid(static_cast<unsigned>(want < 8192 ? want : 8192));
+  const long long rows = static_cast<long long>(B) * t_out;
+  if (rows <= 0) return cudaSuccess;
+  if (rows > (1LL << 30)) return cudaErrorInvalidValue;
+  const long long want = (rows + 7) / 8;  // 8 rows (warps) per block
+  const dim3 grid(static_cast<unsigned>(want < 152 * 16 ? want : 152 * 16));
+  const int r = static_cast<int>(rows);
   if (x_f32 && a_tf32)
-    return launch_pdl(unfold3_kernel<true, true>, grid, dim3(256), 0, stream, x, a, t_in, t_out, C, stride, k_pad, total);
+    return launch_pdl(unfold3_kernel<true, true>, grid, dim3(256), 0, stream, x, a, t_in, t_out, C, stride, k_pad, r);
   if (x_f32)
-    return launch_pdl(unfold3_kernel<true, false>, grid, dim3(256), 0, stream, x, a, t_in, t_out, C, stride, k_pad, total);
-  return launch_pdl(unfold3_kernel<false, false>, grid, dim3(256), 0, stream, x, a, t_in, t_out, C, stride, k_pad, total);
+    return launch_pdl(unfold3_kernel<true, false>, grid, dim3(256), 0, stream, x, a, t_in, t_out, C, stride, k_pad, r);
+  return launch_pdl(unfold3_kernel<false, false>, grid, dim3(256), 0, stream, x, a, t_in, t_out, C, stride, k_pad, r);
 }
 
 cudaError_t launch_conv_weight(const void* w, bool w_bf16, void* wp, bool wp_tf32, int c_out, int c_in, int k_pad,
