@@ -175,6 +175,24 @@ WENC_API wenc_status wenc_encode(wenc* h, const float* mel, float* hidden_out, i
 /* wenc_encode_launches -- kernel launches of one wenc_encode call (-1 without a stem). */
 WENC_API int wenc_encode_launches(const wenc* h);
 
+/* wenc_set_cross_kv -- attach the decoder's cross-attention K/V weights (n_dec_layers >= 1;
+ * wk[l], wv[l]: [d, d] in config.weight_dtype, [n_out, n_in]; bv[l]: [d] float32; all device
+ * pointers owned by the caller). They are packed into one [2 n_dec d, d] matrix in the handle's
+ * precision (K of layer l at rows 2l*d.., V at (2l+1)*d..; K has no bias, as in
+ * turbospark-runtime build_cross_caches). A second call replaces the first. Synchronises
+ * `stream` before returning. Errors: INVALID_ARG (NULL pointers, n_dec_layers < 1), OOM, CUDA. */
+WENC_API wenc_status wenc_set_cross_kv(wenc* h, int n_dec_layers, const void* const* wk, const void* const* wv,
+                                       const float* const* bv, wenc_stream_t stream);
+
+/* wenc_cross_kv -- every decoder layer's cross-attention keys and values over an encoder
+ * output (inferencelayer's cross K/V precompute; turbospark-runtime build_cross_caches):
+ * K_l = enc_out Wk_l^T, V_l = enc_out Wv_l^T + bv_l. enc_out float32 [B, seq_len, d];
+ * kv_out [2 n_dec][B * seq_len][d], plane 2l = K_l and 2l+1 = V_l, in the operand format of the
+ * handle's precision (bf16 for WENC_PREC_BF16, float32 rounded to TF32 for WENC_PREC_TF32),
+ * caller-owned. 1 <= B <= max_batch; buffers 16-byte aligned; needs wenc_set_cross_kv first.
+ * Stream-ordered, 2 launches (the operand cast of enc_out, one GEMM over all layers). */
+WENC_API wenc_status wenc_cross_kv(wenc* h, const float* enc_out, void* kv_out, int B, wenc_stream_t stream);
+
 /* wenc_forward_launches -- number of kernel launches one wenc_forward_layers call with
  * these arguments makes (for launch accounting). Returns -1 on bad arguments. */
 WENC_API int wenc_forward_launches(const wenc* h, int first, int count, int apply_final_ln);
@@ -185,7 +203,8 @@ WENC_API int wenc_forward_launches(const wenc* h, int first, int count, int appl
  * then clears itself. kinds (may be NULL) receives, per launch, 0 = LayerNorm,
  * 1 = QKV GEMM, 2 = attention, 3 = out-proj GEMM, 4 = fc1 GEMM, 5 = fc2 GEMM,
  * 6 = final LayerNorm, 7 = copy, 8 = attention split-key merge (small batches only),
- * 9 = stem unfold, 10 = stem conv1 GEMM, 11 = stem conv2 GEMM (wenc_stem, wenc_encode). */
+ * 9 = stem unfold, 10 = stem conv1 GEMM, 11 = stem conv2 GEMM (wenc_stem, wenc_encode),
+ * 12 = cross K/V operand cast, 13 = cross K/V GEMM (wenc_cross_kv). */
 WENC_API wenc_status wenc_set_launch_events(wenc* h, void* const* events, int n_events, int* kinds);
 
 /* wenc_attention -- out = softmax(q k^T * hd^-0.5) v per (window, head), non-causal,

@@ -31,7 +31,7 @@ import numpy as np
 __all__ = [
     "Workload", "WORKLOADS", "LAYER_KEYS", "MATRIX_KEYS",
     "f32_to_bf16_bits", "bf16_bits_to_f32", "round_to_bf16", "round_to_tf32",
-    "make_layer", "make_weights", "make_input", "make_qkv", "make_stem", "make_mel",
+    "make_layer", "make_weights", "make_input", "make_qkv", "make_stem", "make_mel", "make_cross",
 ]
 
 T_WINDOW = 1500  # encoder positions of one zero-padded 30 s window
@@ -174,6 +174,22 @@ def make_stem(w: Workload) -> dict:
     p["conv2_b"] = _normal(rng, (d,), 0.01)
     p["positions"] = rng.uniform(-1.0, 1.0, (w.seq_len, d)).astype(np.float32)
     return p
+
+
+CROSS_SEED_OFFSET = 104729  # the decoder's cross K/V weights draw from a generator of their own
+
+
+def make_cross(w: Workload, n_dec: int | None = None) -> list:
+    """Decoder cross-attention K/V weights, one dict per decoder layer (n_dec defaults to the
+    encoder's layer count, as in every Whisper size): wk, wv [d, d] ~ N(0, 0.02) (rounded to
+    bf16 for bf16 workloads), bv [d] ~ N(0, 0.01), from PCG64(seed + 104729)."""
+    rng = np.random.Generator(np.random.PCG64(w.seed + CROSS_SEED_OFFSET))
+    mat = (lambda shape: round_to_bf16(_normal(rng, shape, 0.02))) if w.bf16_weights else (lambda shape: _normal(rng, shape, 0.02))
+    d = w.d_model
+    out = []
+    for _ in range(w.n_layers if n_dec is None else n_dec):
+        out.append({"wk": mat((d, d)), "wv": mat((d, d)), "bv": _normal(rng, (d,), 0.01)})
+    return out
 
 
 def make_mel(w: Workload, batch: int | None = None, seed: int = 2) -> np.ndarray:

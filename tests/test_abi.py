@@ -105,3 +105,5 @@ def test_host_side_argument_errors_stem(L):
     assert L.wenc_stem(None, p, p, 1, None) == 1
     assert L.wenc_encode(None, p, p, 1, None) == 1
     assert L.wenc_encode_launches(None) == -1
+    assert L.wenc_set_cross_kv(None, 1, None, None, None, None) == 1
+    assert L.wenc_cross_kv(None, p, p, 1, None) == 1

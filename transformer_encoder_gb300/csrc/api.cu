@@ -226,6 +226,12 @@ struct wenc {
   float *cb1 = nullptr, *cb2 = nullptr, *pos = nullptr;
   void *a1 = nullptr, *h1 = nullptr, *a2 = nullptr;  // unfolded mel, conv1 output, unfolded conv1 output
   CUtensorMap tm_a1, tm_wc1, tm_a2, tm_wc2;
+  // decoder cross K/V weights (wenc_set_cross_kv): [2 n_dec d, d] operand format, bias [2 n_dec d]
+  int n_dec = 0, bn_cross = 0;
+  void* cross_arena = nullptr;
+  void* wx = nullptr;
+  float* bx = nullptr;
+  CUtensorMap tm_wx;
 };
 
 namespace {
@@ -266,6 +272,7 @@ void free_handle(wenc* h) {
   if (h->weight_arena) cudaFree(h->weight_arena);
   if (h->work_arena) cudaFree(h->work_arena);
   if (h->stem_arena) cudaFree(h->stem_arena);
+  if (h->cross_arena) cudaFree(h->cross_arena);
   if (h->err_host) cudaFreeHost(h->err_host);
   delete h;
 }
@@ -730,6 +737,78 @@ wenc_status wenc_encode(wenc* h, const float* mel, float* out, int B, wenc_strea
   enqueue_stem(h, mel, h->x, B, rec);  // the stem writes the residual stream the blocks start from
   if (rec.e == cudaSuccess) enqueue_blocks(h, h->x, out, B, 0, h->cfg.n_layers, h->cfg.final_ln != 0, rec);
   if (rec.e != cudaSuccess) return cuda_fail(rec.e, "encode launch");
+  return WENC_OK;
+}
+
+wenc_status wenc_set_cross_kv(wenc* h, int n_dec, const void* const* wk, const void* const* wv, const float* const* bv,
+                              wenc_stream_t stream_) {
+  g_last_error.clear();
+  if (!h) return fail(WENC_ERR_INVALID_ARG, "handle is NULL");
+  if (n_dec < 1) return fail(WENC_ERR_INVALID_ARG, "n_dec_layers must be >= 1 (got %d)", n_dec);
+  if (!wk || !wv || !bv) return fail(WENC_ERR_INVALID_ARG, "wk/wv/bv arrays are NULL");
+  for (int l = 0; l < n_dec; ++l) {
+    const void* req[] = {wk[l], wv[l], bv[l]};
+    for (const void* p : req) {
+      if (!p) return fail(WENC_ERR_INVALID_ARG, "decoder layer %d: a cross K/V pointer is NULL", l);
+      if (!is_device_accessible(p)) return fail(WENC_ERR_INVALID_ARG, "decoder layer %d: not device memory", l);
+    }
+  }
+  const wenc_config& c = h->cfg;
+  const int d = c.d_model;
+  const size_t es = h->esz, n_out = size_t(2) * n_dec * d;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream_);
+  if (h->cross_arena) {
+    cudaStreamSynchronize(s);
+    cudaFree(h->cross_arena);
+    h->cross_arena = nullptr;
+  }
+  h->n_dec = 0;
+  Arena ar;
+  const size_t o_w = ar.take(n_out * d * es), o_b = ar.take(n_out * 4);
+  cudaError_t e = cudaMalloc(&h->cross_arena, ar.used);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    h->cross_arena = nullptr;
+    return fail(WENC_ERR_OOM, "cross K/V: cudaMalloc(%zu) failed", ar.used);
+  }
+  uint8_t* base = static_cast<uint8_t*>(h->cross_arena);
+  h->wx = base + o_w;
+  h->bx = reinterpret_cast<float*>(base + o_b);
+  const size_t dd = size_t(d) * d;
+  for (int l = 0; l < n_dec && e == cudaSuccess; ++l) {
+    uint8_t* wl = static_cast<uint8_t*>(h->wx) + size_t(2) * l * dd * es;
+    e = pack_matrix(wk[l], c.weight_dtype, h->tf32, wl, dd, s);
+    if (e == cudaSuccess) e = pack_matrix(wv[l], c.weight_dtype, h->tf32, wl + dd * es, dd, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->bx + size_t(2) * l * d, 0, size_t(d) * 4, s);  // K: no bias
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(h->bx + size_t(2 * l + 1) * d, bv[l], size_t(d) * 4, cudaMemcpyDeviceToDevice, s);
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "packing the cross K/V weights");
+  h->bn_cross = wenc_host::gemm_pick_bn(static_cast<int>(n_out));
+  std::string why;
+  const bool ok = h->tf32 ? wenc_host::make_tmap_2d_f32(&h->tm_wx, h->wx, d, n_out, size_t(d) * 4, 32, h->bn_cross, &why)
+                          : wenc_host::make_tmap_2d_bf16(&h->tm_wx, h->wx, d, n_out, size_t(d) * 2, 64, h->bn_cross, &why);
+  if (!ok) return fail(WENC_ERR_CUDA, "%s", why.c_str());
+  h->n_dec = n_dec;
+  return WENC_OK;
+}
+
+wenc_status wenc_cross_kv(wenc* h, const float* enc_out, void* kv_out, int B, wenc_stream_t stream_) {
+  g_last_error.clear();
+  if (!h) return fail(WENC_ERR_INVALID_ARG, "handle is NULL");
+  if (h->n_dec < 1) return fail(WENC_ERR_INVALID_ARG, "no cross K/V weights: call wenc_set_cross_kv first");
+  LaunchRec rec;
+  wenc_status st = begin_call(h, enc_out, kv_out, B, 2, reinterpret_cast<cudaStream_t>(stream_), &rec);
+  if (st != WENC_OK) return st;
+  const int d = h->cfg.d_model, M = B * h->cfg.seq_len;
+  const size_t n = size_t(M) * d;
+  // the encoder output in the operand format, in the LayerNorm-output workspace
+  rec(12, h->tf32 ? wenc_host::launch_to_tf32(enc_out, false, static_cast<float*>(h->xn), n, rec.s)
+                  : wenc_host::launch_f32_to_bf16(enc_out, static_cast<uint16_t*>(h->xn), n, rec.s));
+  rec(13, wenc_host::launch_gemm(h->tm_xn, h->tm_wx, M, 2 * h->n_dec * d, d, h->bn_cross, wenc_host::kEpiBiasPlanes,
+                                 h->bx, nullptr, kv_out, h->err_dev, h->num_sms, rec.s, h->tf32, d));
+  if (rec.e != cudaSuccess) return cuda_fail(rec.e, "cross K/V launch");
   return WENC_OK;
 }
 

@@ -9,6 +9,9 @@
 //   out, fc2: f32  out = resid + (A W^T + b)   (the residual add, in place on x)
 //   conv2:    f32  out = GELU_erf(A W^T + b) + table[row % period]   (the stem's last
 //             convolution with its positional rows, turbospark-runtime encode_partial)
+//   cross K/V: bf16 out = A W^T + b written as planes: columns [p*P, (p+1)*P) of the product go
+//             to plane p, a row-major [M, P] matrix (turbospark-runtime build_cross_caches: one K
+//             and one V matrix per decoder layer)
 // The TF32 form of the kernel takes fp32 A and W (already rounded to TF32 by their producers)
 // and runs kind::tf32 MMAs (128 x BN x 8); its QKV and fc1 outputs are fp32 rounded to TF32.
 //
@@ -96,12 +99,12 @@ __device__ __forceinline__ void load_resid(float4 (&rr)[8], const float* resid, 
 }
 
 // EPI 0 = bias, 1 = bias + GELU, 2 = residual + bias (fp32 out), 3 = GELU(bias) + table row
-// (fp32 out). For EPI 0 and 1 the output is bf16 (F32OUT false) or fp32 rounded to TF32
-// (F32OUT true: the operand of a TF32 GEMM).
+// (fp32 out), 4 = bias with planar output (plane width `plane`). For EPI 0, 1 and 4 the output
+// is bf16 (F32OUT false) or fp32 rounded to TF32 (F32OUT true: the operand of a TF32 GEMM).
 template <int EPI, bool F32OUT>
 __device__ __forceinline__ void epilogue_chunk(const uint32_t (&acc)[32], uint32_t stage, int lane, int grow0, int M,
                                                int N, int col, const float* __restrict__ bias,
-                                               const float4 (&rr)[8], void* out) {
+                                               const float4 (&rr)[8], void* out, int plane) {
 #pragma unroll
   for (int q = 0; q < 8; ++q)
     st_shared_v4(stage_addr(stage, lane, q), acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
@@ -114,7 +117,11 @@ __device__ __forceinline__ void epilogue_chunk(const uint32_t (&acc)[32], uint32
     const float4 a = ld_shared_f4(stage_addr(stage, r, cl));
     const int grow = grow0 + r;
     if (grow < M) {
-      const size_t off = static_cast<size_t>(grow) * N + col + 4 * cl;
+      size_t off = static_cast<size_t>(grow) * N + col + 4 * cl;
+      if constexpr (EPI == 4) {  // the chunk's 32 columns lie in one plane (plane % 32 == 0)
+        const int pl = col / plane;
+        off = (static_cast<size_t>(pl) * M + grow) * plane + (col - pl * plane) + 4 * cl;
+      }
       float4 v = make_float4(a.x + bb.x, a.y + bb.y, a.z + bb.z, a.w + bb.w);
       if constexpr (EPI == 2) {
         v = make_float4(rr[i].x + v.x, rr[i].y + v.y, rr[i].z + v.z, rr[i].w + v.w);
@@ -297,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(tempty_bar(acc));
         }
-        epilogue_chunk<EPI, TF32>(r, stage, lane, grow0, M, N, c0 + c * 32, bias, rb[c & 1], out);
+        epilogue_chunk<EPI, TF32>(r, stage, lane, grow0, M, N, c0 + c * 32, bias, rb[c & 1], out, row_period);
         if constexpr (kRowInput) {
           if (c + 2 < CH) {
             load_resid(rb[c & 1], resid, grow0, M, N, c0 + (c + 2) * 32, lane, row_period);
@@ -352,6 +359,7 @@ cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmW, int M, i
                         cudaStream_t stream, bool tf32, int row_period) {
   if (M <= 0) return cudaSuccess;
   if (epilogue == 3 && row_period <= 0) return cudaErrorInvalidValue;
+  if (epilogue == 4 && (row_period <= 0 || row_period % 32 != 0 || N % row_period != 0)) return cudaErrorInvalidValue;
 #define WENC_GEMM_CASE(BNV, EPIV, TF) \
   if (bn == BNV && epilogue == EPIV && tf32 == TF)                                        \
     return launch_one<BNV, EPIV, TF>(tmA, tmW, M, N, K, bias, resid, out, err, num_sms, stream, row_period);
@@ -363,6 +371,8 @@ cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmW, int M, i
   WENC_GEMM_CASE(128, 2, false)
   WENC_GEMM_CASE(256, 3, false)
   WENC_GEMM_CASE(128, 3, false)
+  WENC_GEMM_CASE(256, 4, false)
+  WENC_GEMM_CASE(128, 4, false)
   WENC_GEMM_CASE(256, 0, true)
   WENC_GEMM_CASE(256, 1, true)
   WENC_GEMM_CASE(256, 2, true)
@@ -371,6 +381,8 @@ cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmW, int M, i
   WENC_GEMM_CASE(128, 2, true)
   WENC_GEMM_CASE(256, 3, true)
   WENC_GEMM_CASE(128, 3, true)
+  WENC_GEMM_CASE(256, 4, true)
+  WENC_GEMM_CASE(128, 4, true)
 #undef WENC_GEMM_CASE
   return cudaErrorInvalidValue;
 }

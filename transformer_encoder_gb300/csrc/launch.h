@@ -64,6 +64,9 @@ constexpr int kGemmBK = 64;
 // Epilogue 3 (internal, the stem's conv2): out fp32 = GELU_erf(A W^T + bias) + resid[row % row_period]
 // with resid a [row_period, N] fp32 table (row_period > 0).
 constexpr int kEpiGeluTable = 3;
+// Epilogue 4 (internal, the cross K/V precompute): as epilogue 0, written as planes of width
+// row_period: out[(col / P) * M * P + row * P + col % P]. P % 32 == 0 and N % P == 0.
+constexpr int kEpiBiasPlanes = 4;
 cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmW, int M, int N, int K, int bn, int epilogue,
                         const float* bias, const float* resid, void* out, uint32_t* err, int num_sms,
                         cudaStream_t stream, bool tf32 = false, int row_period = 0);

@@ -25,13 +25,14 @@ PREC_BF16, PREC_TF32 = 0, 1
 _STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "OOM", 4: "CUDA", 5: "DEVICE_TIMEOUT"}
 LAUNCH_KINDS = {0: "layernorm", 1: "gemm_qkv", 2: "attention", 3: "gemm_out", 4: "gemm_fc1", 5: "gemm_fc2",
                 6: "layernorm_final", 7: "copy", 8: "attention_combine", 9: "stem_unfold", 10: "gemm_conv1",
-                11: "gemm_conv2"}
+                11: "gemm_conv2", 12: "cross_kv_cast", 13: "gemm_cross_kv"}
 
 EXPORTED_SYMBOLS = (
     "wenc_create", "wenc_forward", "wenc_forward_layers", "wenc_forward_launches", "wenc_set_launch_events",
     "wenc_attention", "wenc_layernorm", "wenc_linear", "wenc_sync_status", "wenc_destroy", "wenc_last_error",
     "wenc_version", "wenc_selftest_wait_timeout", "wenc_attention_static", "wenc_attention_static_capacity",
     "wenc_linear_tf32", "wenc_attention_tf32", "wenc_set_stem", "wenc_stem", "wenc_encode", "wenc_encode_launches",
+    "wenc_set_cross_kv", "wenc_cross_kv",
 )
 
 
@@ -86,6 +87,8 @@ def lib() -> ctypes.CDLL:
         L.wenc_stem.argtypes = [vp, vp, vp, i, vp]
         L.wenc_encode.argtypes = [vp, vp, vp, i, vp]
         L.wenc_encode_launches.argtypes = [vp]
+        L.wenc_set_cross_kv.argtypes = [vp, i, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp), vp]
+        L.wenc_cross_kv.argtypes = [vp, vp, vp, i, vp]
         L.wenc_attention_tf32.argtypes = [vp, vp, vp, vp, i, i, i, i, vp]
         L.wenc_sync_status.argtypes = [vp]
         L.wenc_selftest_wait_timeout.argtypes = [vp]
@@ -100,7 +103,7 @@ def lib() -> ctypes.CDLL:
         for name in ("wenc_create", "wenc_forward", "wenc_forward_layers", "wenc_set_launch_events", "wenc_attention",
                      "wenc_layernorm", "wenc_linear", "wenc_sync_status", "wenc_forward_launches",
                      "wenc_selftest_wait_timeout", "wenc_linear_tf32", "wenc_attention_tf32", "wenc_set_stem",
-                     "wenc_stem", "wenc_encode", "wenc_encode_launches"):
+                     "wenc_stem", "wenc_encode", "wenc_encode_launches", "wenc_set_cross_kv", "wenc_cross_kv"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -155,6 +158,7 @@ class Encoder:
         cfg = Config(len(layers), d, n_heads, d // n_heads, f, seq_len, max_batch, 1 if final is not None else 0,
                      ln_eps, 1 if mdtype == torch.bfloat16 else 0, PREC_TF32 if precision == "tf32" else PREC_BF16)
         self.precision = precision
+        self.n_dec = 0  # decoder layers of the cross K/V weights (set_cross_kv)
         arr = (LayerWeights * len(layers))()
         for i, p in enumerate(layers):
             for k in ("wq", "wk", "wv", "wo", "w1", "w2"):
@@ -227,6 +231,36 @@ class Encoder:
             out = torch.empty((mel.shape[0], self.seq_len, self.d_model), dtype=torch.float32, device=mel.device)
         _require(out, torch.float32, "out")
         _check(lib().wenc_encode(self._h, _ptr(mel), _ptr(out), mel.shape[0], _stream(stream)))
+        return out
+
+    def set_cross_kv(self, dec_layers, stream=None):
+        """Attach the decoder's cross-attention K/V weights: a list (one per decoder layer) of
+        dicts with wk, wv ([d, d], the layers' matrix dtype) and bv ([d] float32) CUDA tensors."""
+        import torch
+        mdtype = torch.bfloat16 if self.cfg.weight_dtype == 1 else torch.float32
+        n = len(dec_layers)
+        for p in dec_layers:
+            _require(p["wk"], mdtype, "wk")
+            _require(p["wv"], mdtype, "wv")
+            _require(p["bv"], torch.float32, "bv")
+        arr = lambda key: (ctypes.c_void_p * n)(*[p[key].data_ptr() for p in dec_layers])
+        wk, wv, bv = arr("wk"), arr("wv"), arr("bv")
+        _check(lib().wenc_set_cross_kv(self._h, n, wk, wv, bv, _stream(stream)))
+        self.n_dec = n
+
+    def cross_kv(self, enc_out, out=None, stream=None):
+        """[2 n_dec, B * seq_len, d] cross K/V planes (K of layer l at 2l, V at 2l + 1) of an
+        encoder output float32 [B, seq_len, d]; bf16 for the bf16 precision, float32 for TF32."""
+        import torch
+        _require(enc_out, torch.float32, "enc_out")
+        B = enc_out.shape[0]
+        dt = torch.float32 if self.precision == "tf32" else torch.bfloat16
+        if self.n_dec == 0:  # the library reports the missing weights
+            _check(lib().wenc_cross_kv(self._h, _ptr(enc_out), None, B, _stream(stream)))
+        if out is None:
+            out = torch.empty((2 * self.n_dec, B * self.seq_len, self.d_model), dtype=dt, device=enc_out.device)
+        _require(out, dt, "out")
+        _check(lib().wenc_cross_kv(self._h, _ptr(enc_out), _ptr(out), B, _stream(stream)))
         return out
 
     def encode_launches(self) -> int:
