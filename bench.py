@@ -15,6 +15,10 @@ there is no collective on the data path): value = all ranks' windows / the slowe
 `--stem` makes a step the whole encoder from log-mel frames (wenc_encode: the convolutional stem,
 the blocks and the final LayerNorm) with the input [B, 3000, n_mels] on the device.
 
+`--cross-kv` adds to each step the decoder's cross-attention K/V precompute over the encoder
+output (wenc_cross_kv: 2 x n_layers decoder projections, one GEMM); `e2e` still reads back the
+encoder output, not the K/V planes, which a decoder consumes on the device.
+
 `--precision tf32` runs the same step with TF32 tensor-core operands and fp32 activations; its
 roofline peak is the measured bf16 peak times the nominal TF32/BF16 ratio (1.1 / 2.25 PFLOP/s).
 
@@ -223,6 +227,19 @@ def stem_flops(w) -> float:
     return 2.0 * w.batch * (2 * T * d * 3 * w.n_mels + T * d * 3 * d)
 
 
+def time_oracle_cross(w, n_dec: int = 2):
+    """Seconds of the f64 oracle's cross K/V precompute for one window and n_dec decoder layers."""
+    import numpy as np
+
+    import oracle
+    import synth
+    dec = synth.make_cross(w, n_dec)
+    x = np.random.default_rng(0).standard_normal((w.seq_len, w.d_model))
+    t0 = time.perf_counter()
+    oracle.cross_kv(x, [p["wk"] for p in dec], [p["wv"] for p in dec], [p["bv"] for p in dec])
+    return time.perf_counter() - t0
+
+
 def host_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -230,12 +247,15 @@ def host_cores():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(w, seconds: float, with_stem: bool = False):
+def cpu_baseline(w, seconds: float, with_stem: bool = False, with_cross: bool = False):
     times = time_oracle_block(w, seconds)
     t_block = statistics.median(times)
     t_stem = statistics.median(time_oracle_stem(w, 3)) if with_stem else 0.0
-    win_s = 1.0 / (t_block * w.n_layers + t_stem)
+    t_cross = time_oracle_cross(w, 2) * w.n_layers / 2 if with_cross else 0.0
+    win_s = 1.0 / (t_block * w.n_layers + t_stem + t_cross)
     stem_note = f" + the stem ({t_stem:.3f} s, median of 3)" if with_stem else ""
+    if with_cross:
+        stem_note += f" + cross K/V of 2 decoder layers x{w.n_layers / 2:g} ({t_cross:.3f} s)"
     return {"value": win_s, "unit": "windows/s", "cores": host_cores(), "kind": "oracle",
             "sample": (f"f64 numpy oracle, one block of one {w.seq_len}-frame window at {w.name} dims, "
                        f"median of {len(times)} runs ({t_block:.3f} s/block), extrapolated x{w.n_layers} blocks"
@@ -316,6 +336,19 @@ def run_wenc(args, w):
         x_host = torch.from_numpy(synth.make_input(w, rng)).pin_memory()
         step = enc.forward
         n_launch = enc.launches()
+    if args.cross_kv:
+        mdt = torch.bfloat16 if w.bf16_weights else torch.float32
+        enc.set_cross_kv([{"wk": torch.from_numpy(p["wk"]).to(mdt).cuda(), "wv": torch.from_numpy(p["wv"]).to(mdt).cuda(),
+                           "bv": torch.from_numpy(p["bv"]).cuda()} for p in synth.make_cross(w)])
+        kv = torch.empty((2 * w.n_layers, w.batch * w.seq_len, w.d_model),
+                         dtype=torch.float32 if tf32 else torch.bfloat16, device="cuda")
+        base_step = step
+        n_base = n_launch
+
+        def step(x_, out_):
+            base_step(x_, out_)
+            enc.cross_kv(out_, kv)
+        n_launch += 2
     x = x_host.cuda()
     out = torch.empty((w.batch, w.seq_len, w.d_model), dtype=torch.float32, device="cuda")
     out_host = torch.empty(tuple(out.shape), dtype=torch.float32).pin_memory()
@@ -342,8 +375,17 @@ def run_wenc(args, w):
     t_stop = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for k in range(args.steps):
-        ks = enc.set_launch_events(ev[k])
-        step(x, out)
+        if args.cross_kv:
+            # the timing hook covers one library call: arm it for the encoder, then for the
+            # cross K/V call (whose first event repeats the encoder's last one)
+            ks1 = enc.set_launch_events(ev[k][:n_base + 1])
+            base_step(x, out)
+            ks2 = enc.set_launch_events(ev[k][n_base:])
+            enc.cross_kv(out, kv)
+            ks = list(ks1)[:n_base] + list(ks2)[:2]
+        else:
+            ks = enc.set_launch_events(ev[k])
+            step(x, out)
         if kinds is None:
             kinds = ks
     t_stop.record(stream)
@@ -386,7 +428,8 @@ def run_wenc(args, w):
     ms_step = ms_total / args.steps
     windows = w.batch * world
     value = job_throughput(w.batch, world, args.steps, ms_total)
-    flops_step = w.flops() + (stem_flops(w) if args.stem else 0.0)
+    cross_flops = 2.0 * w.batch * w.seq_len * (2 * w.n_layers * w.d_model) * w.d_model
+    flops_step = w.flops() + (stem_flops(w) if args.stem else 0.0) + (cross_flops if args.cross_kv else 0.0)
     tflops = flops_step * world / (ms_step / 1e3) / 1e12
 
     # ---- roofline of the dominant kernel (the tcgen05 GEMM: four launches per block)
@@ -410,6 +453,10 @@ def run_wenc(args, w):
             kern[name] = {"launches": n, "avg_us": 1e3 * avg, "tflops": attn_flops / (avg / 1e3) / 1e12}
         elif name in stem_gemm_flops:
             kern[name] = {"launches": n, "avg_us": 1e3 * avg, "tflops": stem_gemm_flops[name] / (avg / 1e3) / 1e12}
+        elif name == "gemm_cross_kv":
+            kern[name] = {"launches": n, "avg_us": 1e3 * avg, "tflops": cross_flops / (avg / 1e3) / 1e12}
+        elif name == "cross_kv_cast":
+            kern[name] = {"launches": n, "avg_us": 1e3 * avg, "gbs": M * d * (4 + es) / (avg / 1e3) / 1e9}
         elif name == "stem_unfold":
             kern[name] = {"launches": n, "avg_us": 1e3 * avg, "gbs": unfold_bytes * args.steps / (ms / 1e3) / 1e9}
         elif name in ("layernorm", "layernorm_final"):
@@ -445,7 +492,9 @@ def run_wenc(args, w):
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "tf32" if tf32 else "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(w) + (f", from {2 * T} log-mel frames x {w.n_mels} through the "
-                                                   "convolutional stem" if args.stem else ""),
+                                                   "convolutional stem" if args.stem else "")
+                   + (f", plus the cross-attention K/V of {w.n_layers} decoder layers (e2e reads back the encoder "
+                      "output only)" if args.cross_kv else ""),
                    "windows_per_step": w.batch, "seq_len": T,
                    "l2": "no flush: each step streams 1.26 GB of weights and >400 MB of activations, above the 126 MB L2"
                    if w.name == "large_stack" else "no flush",
@@ -462,7 +511,7 @@ def run_wenc(args, w):
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, with_stem=args.stem)
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, with_stem=args.stem, with_cross=args.cross_kv)
     if rank == 0:
         print(json.dumps(line), flush=True)
     enc.close()
@@ -481,6 +530,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="large_stack")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle's CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cross-kv", action="store_true",
+                    help="add the decoder cross-attention K/V precompute over the encoder output to each step")
     ap.add_argument("--stem", action="store_true",
                     help="time the whole encoder from log-mel frames (convolutional stem + blocks)")
     ap.add_argument("--precision", choices=("bf16", "tf32"), default="bf16",

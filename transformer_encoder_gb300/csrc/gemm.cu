@@ -173,6 +173,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int m_tiles = (M + BM - 1) / BM;
   const int n_tiles = N / BN;
   const int num_tiles = m_tiles * n_tiles;
+  // Tile order. The block GEMMs walk n fastest: a wave of CTAs shares one A row block, and W
+  // (at most 13 MB) stays in L2. The cross K/V product's W spans every decoder layer (210 MB at
+  // large-v3 dims) and its 3.9 GB output streams through L2, so it walks groups of kGroupM row
+  // blocks: within a group m is fastest, and the group sweeps every column block before the
+  // next group starts. A wave then shares a few W tiles, the group's slice of A (64 x 128 rows)
+  // stays in L2, and W is read m_tiles / kGroupM times instead of once per row block.
+  constexpr bool kGrouped = (EPI == 4);
+  constexpr int kGroupM = 64;
+  auto tile_m = [&](int t) {
+    if constexpr (!kGrouped) return t / n_tiles;
+    const int g = t / (kGroupM * n_tiles), first = g * kGroupM;
+    const int gs = min(kGroupM, m_tiles - first);
+    return first + (t - g * kGroupM * n_tiles) % gs;
+  };
+  auto tile_n = [&](int t) {
+    if constexpr (!kGrouped) return t % n_tiles;
+    const int g = t / (kGroupM * n_tiles), first = g * kGroupM;
+    const int gs = min(kGroupM, m_tiles - first);
+    return (t - g * kGroupM * n_tiles) / gs;
+  };
   constexpr int BKE = TF32 ? 32 : BK;  // K elements per stage (128-byte rows)
   const int k_blocks = K / BKE;
 
@@ -209,8 +229,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t issued_mask = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-      const int m0 = (tile / n_tiles) * BM;
-      const int n0 = (tile % n_tiles) * BN;
+      const int m0 = tile_m(tile) * BM;
+      const int n0 = tile_n(tile) * BN;
       for (int kb = 0; kb < k_blocks; ++kb) {
         if (!mbar_wait(empty_bar(stage), phase ^ 1u, wc, 1)) { ok = false; break; }
         mbar_arrive_expect_tx(full_bar(stage), C::STAGE_BYTES);
@@ -274,8 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;
     const int col_half = (warp - 2) >> 2;
     const uint32_t stage = smem_u32(smem + STAGES * C::STAGE_BYTES) + (warp - 2) * C::EPI_STAGE_BYTES;
-    auto row0_of = [&](int t) { return (t / n_tiles) * BM + quad * 32; };
-    auto col_of = [&](int t) { return (t % n_tiles) * BN + col_half * (BN / 2); };
+    auto row0_of = [&](int t) { return tile_m(t) * BM + quad * 32; };
+    auto col_of = [&](int t) { return tile_n(t) * BN + col_half * (BN / 2); };
     float4 rb[2][8];
     constexpr bool kRowInput = (EPI == 2 || EPI == 3);  // residual rows or table rows
     if constexpr (kRowInput) {

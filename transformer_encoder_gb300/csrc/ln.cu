@@ -86,19 +86,47 @@ cudaError_t launch_nv(const float* x, const float* w, const float* b, void* y, i
   return wenc_host::launch_pdl(layernorm_kernel<NV, 0>, dim3(grid), block, 0, stream, x, w, b, y, rows, eps);
 }
 
-__global__ void f32_to_bf16_kernel(const float* __restrict__ src, uint16_t* __restrict__ dst, size_t n) {
-  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    __nv_bfloat16 v = __float2bfloat16_rn(src[i]);  // round to nearest, ties to even
+// fp32 -> bf16, round to nearest with ties to even. Eight elements per thread and iteration
+// (two 16-byte loads, one 16-byte store) when n and both pointers allow it, else one.
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+  const __nv_bfloat16 a = __float2bfloat16_rn(lo), b = __float2bfloat16_rn(hi);
+  return static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&a)) |
+         (static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&b)) << 16);
+}
+
+__global__ void f32_to_bf16_kernel(const float* __restrict__ src, uint16_t* __restrict__ dst, size_t n, int vec8) {
+  const size_t tid = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x;
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  if (vec8) {
+    for (size_t i = tid; i < n / 8; i += stride) {
+      const float4 a = reinterpret_cast<const float4*>(src)[2 * i];
+      const float4 b = reinterpret_cast<const float4*>(src)[2 * i + 1];
+      reinterpret_cast<uint4*>(dst)[i] =
+          make_uint4(bf16x2_rn(a.x, a.y), bf16x2_rn(a.z, a.w), bf16x2_rn(b.x, b.y), bf16x2_rn(b.z, b.w));
+    }
+    return;
+  }
+  for (size_t i = tid; i < n; i += stride) {
+    __nv_bfloat16 v = __float2bfloat16_rn(src[i]);
     dst[i] = *reinterpret_cast<uint16_t*>(&v);
   }
 }
 
 // Weight packing for the TF32 path: fp32 matrices are rounded to TF32 (nearest, ties away
 // from zero); bf16 matrices are widened, which is exact (bf16 has fewer mantissa bits).
-__global__ void to_tf32_kernel(const void* __restrict__ src, int src_bf16, float* __restrict__ dst, size_t n) {
-  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+__global__ void to_tf32_kernel(const void* __restrict__ src, int src_bf16, float* __restrict__ dst, size_t n,
+                               int vec4) {
+  const size_t tid = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x;
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  if (vec4 && !src_bf16) {  // four fp32 elements per thread and iteration
+    for (size_t i = tid; i < n / 4; i += stride) {
+      const float4 a = reinterpret_cast<const float4*>(src)[i];
+      reinterpret_cast<float4*>(dst)[i] = make_float4(wenc_dev::round_tf32(a.x), wenc_dev::round_tf32(a.y),
+                                                      wenc_dev::round_tf32(a.z), wenc_dev::round_tf32(a.w));
+    }
+    return;
+  }
+  for (size_t i = tid; i < n; i += stride) {
     if (src_bf16)
       dst[i] = __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t*>(src)[i]) << 16);
     else
@@ -129,15 +157,21 @@ cudaError_t launch_layernorm(const float* x, const float* w, const float* b, voi
 
 cudaError_t launch_f32_to_bf16(const float* src, uint16_t* dst, size_t n, cudaStream_t stream) {
   if (n == 0) return cudaSuccess;
-  const size_t blocks = (n + 255) / 256;
-  f32_to_bf16_kernel<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(src, dst, n);
+  const bool vec8 = n % 8 == 0 && (reinterpret_cast<uintptr_t>(src) & 15u) == 0 &&
+                    (reinterpret_cast<uintptr_t>(dst) & 15u) == 0;
+  const size_t blocks = ((vec8 ? n / 8 : n) + 255) / 256;
+  f32_to_bf16_kernel<<<static_cast<unsigned>(blocks < 152 * 16 ? blocks : 152 * 16), 256, 0, stream>>>(src, dst, n,
+                                                                                                   vec8 ? 1 : 0);
   return cudaGetLastError();
 }
 
 cudaError_t launch_to_tf32(const void* src, bool src_bf16, float* dst, size_t n, cudaStream_t stream) {
   if (n == 0) return cudaSuccess;
-  const size_t blocks = (n + 255) / 256;
-  to_tf32_kernel<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(src, src_bf16 ? 1 : 0, dst, n);
+  const bool vec4 = !src_bf16 && n % 4 == 0 && (reinterpret_cast<uintptr_t>(src) & 15u) == 0 &&
+                    (reinterpret_cast<uintptr_t>(dst) & 15u) == 0;
+  const size_t blocks = ((vec4 ? n / 4 : n) + 255) / 256;
+  to_tf32_kernel<<<static_cast<unsigned>(blocks < 152 * 16 ? blocks : 152 * 16), 256, 0, stream>>>(
+      src, src_bf16 ? 1 : 0, dst, n, vec4 ? 1 : 0);
   return cudaGetLastError();
 }
 
