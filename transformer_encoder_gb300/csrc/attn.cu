@@ -11,12 +11,14 @@
 //    rings of their own, in the order the tensor pipe consumes them;
 //  - one thread of warp 1 issues S_A = Q_A K_j^T and S_B = Q_B K_j^T (M128 N128 K64, into TMEM)
 //    as soon as the scores of tile j-1 have been read; one thread each of warps 2 and 3 issues
-//    O_A += P_A V_j and O_B += P_B V_j (M128 N64, V read MN-major, O accumulated in TMEM) once P
+//    O_A += P_A V_j and O_B += P_B V_j (M128 N64, P from TMEM, V read MN-major from shared
+//    memory, O accumulated in TMEM) once P
 //    of tile j is written (one issuing thread cannot keep the tensor pipe fed with N = 64 MMAs);
 //  - warps 4-7 (tile A) and 8-11 (tile B) own one query row per thread: they read the row's 128
 //    scores from TMEM, keep the running maximum and denominator in registers (the online-softmax
-//    recurrence of VANILLA_ATTN, in base 2 with hd^-0.5*log2(e) folded in), write P as bf16 into
-//    128-byte-swizzled shared memory and rescale O in TMEM when the running maximum moves by more
+//    recurrence of VANILLA_ATTN, in base 2 with hd^-0.5*log2(e) folded in), write P as bf16 pairs
+//    into the tile's P columns of TMEM (the PV product reads its A operand from there: no P
+//    traffic through shared memory) and rescale O in TMEM when the running maximum moves by more
 //    than 2^8. The two tiles take turns on the exponentials (ping-pong), so one tile's exps run
 //    while the other tile loads scores, stores P or waits, and the tensor pipe runs the other
 //    tile's products meanwhile. No T x T score buffer exists.
@@ -31,6 +33,18 @@ namespace {
 
 using namespace wenc_dev;
 
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16 with bf16 operands; A = 128 lanes x 8 columns, each
+// 32-bit column holding two consecutive K elements (the lower one in the low half).
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 constexpr int BQ = wenc_host::kAttnBQ;    // query rows per tile (two tiles per CTA)
 constexpr int BKV = wenc_host::kAttnBKV;  // keys per tile
 constexpr int HD = 64;
@@ -39,19 +53,16 @@ constexpr int NV = 3;                     // V ring depth
 constexpr int kThreads = 384;             // producer, 3 MMA issuers, 2 softmax warpgroups
 
 constexpr uint32_t Q_BYTES = BQ * HD * 2;           // 16 KB per query tile
-constexpr uint32_t P_HALF = BQ * 64 * 2;            // 16 KB: 128 rows x 64 keys, one swizzle-atom column
-constexpr uint32_t P_BYTES = 2 * P_HALF;            // 32 KB per query tile
 constexpr uint32_t KV_BYTES = BKV * HD * 2;         // 16 KB per K or V tile
 constexpr uint32_t OFF_Q = 0;                       // Q_A, Q_B
-constexpr uint32_t OFF_P = OFF_Q + 2 * Q_BYTES;     // P_A, P_B
-constexpr uint32_t OFF_K = OFF_P + 2 * P_BYTES;
+constexpr uint32_t OFF_K = OFF_Q + 2 * Q_BYTES;
 constexpr uint32_t OFF_V = OFF_K + NK * KV_BYTES;
 constexpr uint32_t OFF_BARS = OFF_V + NV * KV_BYTES;
 // bars: q_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], and per query tile t:
 // s_full[t], s_free[t], p_full[t], pv_done[t], turn[t]; drain
 constexpr int NUM_BARS = 1 + 2 * NK + 2 * NV + 10 + 1;
 constexpr size_t SMEM = 1024 + OFF_BARS + NUM_BARS * 8 + 16;
-constexpr uint32_t TMEM_COLS = 512;  // S_A 0..127, S_B 128..255, O_A 256..319, O_B 320..383
+constexpr uint32_t TMEM_COLS = 512;  // S_A 0..127, S_B 128..255, O_A 256..319, O_B 320..383, P_A 384..447, P_B 448..511
 // Grow the running maximum only when a tile's maximum exceeds it by more than this (log2
 // units); otherwise keep it, so p <= 2^8 and O is rescaled rarely. The result is unchanged:
 // numerator and denominator always use the same reference maximum.
@@ -65,7 +76,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s0 = smem_u32(smem);
-  const uint32_t sQ = s0 + OFF_Q, sP = s0 + OFF_P, sK = s0 + OFF_K, sV = s0 + OFF_V;
+  const uint32_t sQ = s0 + OFF_Q, sK = s0 + OFF_K, sV = s0 + OFF_V;
   const uint32_t bar0 = s0 + OFF_BARS;
   const uint32_t q_full = bar0;
   auto k_full = [&](int s) { return bar0 + 8u * (1 + s); };
@@ -130,6 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_wait();     // Q, K, V from the previous kernel are complete from here on
   auto tS = [&](int t) { return tmem_base + 128u * t; };
   auto tO = [&](int t) { return tmem_base + 256u + 64u * t; };
+  auto tP = [&](int t) { return tmem_base + 384u + 64u * t; };  // P as bf16 pairs: 64 columns per tile
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer: Q_A, Q_B; then K0, then (K[j], V[j-1]) for j >= 1, then V[n-1]
@@ -192,7 +204,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
       constexpr uint32_t idesc_o = idesc_bf16_f32(BQ, HD, true);  // B = V tile, MN-major, N = 64
       const int t = warp - 2;
-      const uint64_t pdesc = sdesc_sw128(sP + t * P_BYTES, 16, 1024);
       for (int j = 0; ok && j < n_kv; ++j) {
         const int st = j % NV;
         if (!mbar_wait(v_full(st), (j / NV) & 1, wc, 15)) break;
@@ -201,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t vdesc = sdesc_sw128(sV + st * KV_BYTES, 1024, 1024);
 #pragma unroll
         for (int k = 0; k < BKV / 16; ++k)
-          umma_bf16_ss(tO(t), pdesc + (k >> 2) * (P_HALF >> 4) + (k & 3) * 2, vdesc + k * 128, idesc_o,
+          umma_bf16_ts(tO(t), tP(t) + 8 * k, vdesc + k * 128, idesc_o,
                        (j > 0 || k > 0) ? 1u : 0u);
         umma_commit(pv_done(t));
         umma_commit(v_empty(st));
@@ -216,7 +227,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t prow = sP + t * P_BYTES + row * 128;
     float m = -CUDART_INF_F;  // running maximum, in units of scale_log2
     float l = 0.0f;           // running denominator
     bool ok = true;
@@ -302,17 +312,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
 
-      // P row (128 keys) as two 64-key halves, each a K-major 128-byte-swizzled 128 x 64 tile.
+      // P row (128 keys as 64 bf16 pairs) into the tile's P columns of TMEM.
+      {
+        uint32_t p0[32], p1[32];
 #pragma unroll
-      for (int c8 = 0; c8 < 16; ++c8) {
-        const uint32_t addr = prow + (c8 >> 3) * P_HALF + (((c8 & 7) ^ (row & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * c8]), "r"(pk[4 * c8 + 1]),
-                     "r"(pk[4 * c8 + 2]), "r"(pk[4 * c8 + 3])
-                     : "memory");
+        for (int e = 0; e < 32; ++e) {
+          p0[e] = pk[e];
+          p1[e] = pk[32 + e];
+        }
+        tmem_st_32x32b_x32(tP(t) + lane_off, p0);
+        tmem_st_32x32b_x32(tP(t) + lane_off + 32, p1);
+        tmem_st_wait();
       }
       l = l * alpha + sum;
       m = m_new;
-      fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full(t));
