@@ -457,6 +457,8 @@ def run_wenc(args, w):
             kern[name] = {"launches": n, "avg_us": 1e3 * avg, "tflops": cross_flops / (avg / 1e3) / 1e12}
         elif name == "cross_kv_cast":
             kern[name] = {"launches": n, "avg_us": 1e3 * avg, "gbs": M * d * (4 + es) / (avg / 1e3) / 1e9}
+        elif name == "row_stats":
+            kern[name] = {"launches": n, "avg_us": 1e3 * avg, "gbs": 6.0 * M * d / (avg / 1e3) / 1e9}
         elif name == "stem_unfold":
             kern[name] = {"launches": n, "avg_us": 1e3 * avg, "gbs": unfold_bytes * args.steps / (ms / 1e3) / 1e9}
         elif name in ("layernorm", "layernorm_final"):

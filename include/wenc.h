@@ -204,7 +204,8 @@ WENC_API int wenc_forward_launches(const wenc* h, int first, int count, int appl
  * 1 = QKV GEMM, 2 = attention, 3 = out-proj GEMM, 4 = fc1 GEMM, 5 = fc2 GEMM,
  * 6 = final LayerNorm, 7 = copy, 8 = attention split-key merge (small batches only),
  * 9 = stem unfold, 10 = stem conv1 GEMM, 11 = stem conv2 GEMM (wenc_stem, wenc_encode),
- * 12 = cross K/V operand cast, 13 = cross K/V GEMM (wenc_cross_kv). */
+ * 12 = cross K/V operand cast, 13 = cross K/V GEMM (wenc_cross_kv), 14 = row statistics of the
+ * first block's input (BF16 precision, which folds LN1 into the QKV GEMM: kind 0 is then LN2). */
 WENC_API wenc_status wenc_set_launch_events(wenc* h, void* const* events, int n_events, int* kinds);
 
 /* wenc_attention -- out = softmax(q k^T * hd^-0.5) v per (window, head), non-causal,

@@ -170,7 +170,8 @@ def test_split_key_attention_edge_shape():
     from dataclasses import replace
     w = replace(synth.WORKLOADS["tiny_block"], name="split_edge", d_model=128, n_heads=2, ffn_dim=256, seq_len=700)
     enc, layers, _, rng = make_encoder(w)
-    assert enc.launches() == 8  # seven block launches plus the split-key merge
+    # row statistics, QKV (LN1 folded), attention, the split-key merge, out-proj, LN2, fc1, fc2
+    assert enc.launches() == 8
     x = synth.make_input(w, rng)
     y = enc.forward(_t(x))
     torch.cuda.synchronize()

@@ -136,6 +136,6 @@ def test_encode_launch_accounting_and_errors():
     kinds = enc.set_launch_events(events)
     enc.encode(mel)
     torch.cuda.synchronize()
-    assert list(kinds)[:5] == [9, 10, 9, 11, 0]
+    assert list(kinds)[:5] == [9, 10, 9, 11, 14]  # the stem, then the blocks' row statistics
     with pytest.raises(WencError):
         enc.encode(_t(synth.make_mel(w, batch=2)))  # B above max_batch

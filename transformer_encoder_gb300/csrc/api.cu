@@ -198,6 +198,9 @@ struct wenc {
   struct Layer {
     void *wqkv, *wo, *w1, *w2;  // [n_out, n_in], bf16 or TF32-rounded fp32
     float *ln1_w, *ln1_b, *bqkv, *bo, *ln2_w, *ln2_b, *b1, *b2;
+    // BF16 precision: LN1 is folded into Wqkv (wqkv and bqkv hold the folded forms) and this
+    // holds the row sums of the folded matrix; null for TF32
+    float* cs_qkv = nullptr;
     CUtensorMap tm_wqkv, tm_wo, tm_w1, tm_w2;
   };
   std::vector<Layer> layers;
@@ -209,6 +212,8 @@ struct wenc {
   void *xn = nullptr, *qkv = nullptr, *o = nullptr, *u = nullptr;  // element size esz
   CUtensorMap tm_xn, tm_o, tm_u, tm_q, tm_kv;
   int attn_splits = 1;            // key splits of the attention (1 = none), fixed at create
+  float2* stats = nullptr;        // BF16: row segment statistics of the residual stream (workspace)
+  int seg_w = 0;                  // their segment width
   float* part_o = nullptr;        // split-key partial numerators (workspace)
   float2* part_ml = nullptr;      // split-key (max, sum) pairs (workspace)
   void* weight_arena = nullptr;
@@ -350,6 +355,8 @@ void enqueue_blocks(wenc* h, const float* in, float* out, int B, int first, int 
   const int d = c.d_model, f = c.ffn_dim, T = c.seq_len, H = c.n_heads;
   const int M = B * T;
   const float* src = in;  // the residual stream entering the next block
+  if (!h->tf32 && count > 0)  // statistics and bf16 copy of the first block's input
+    rec(14, wenc_host::launch_row_stats(in, static_cast<uint16_t*>(h->xn), h->stats, M, d, h->seg_w, s));
   for (int l = first; l < first + count && rec.e == cudaSuccess; ++l) {
     const wenc::Layer& P = h->layers[l];
     const bool last = (l == first + count - 1);
@@ -371,10 +378,21 @@ void enqueue_blocks(wenc* h, const float* in, float* out, int B, int first, int 
       src = h->x;
       continue;
     }
+    // BF16: LN1 is folded into the QKV GEMM, which reads the raw residual stream (its bf16 copy
+    // in xn) and the row statistics written by the previous block's fc2 epilogue (or, for the
+    // call's first block, by the row-statistics kernel). LN2 stays a kernel of its own: folding
+    // it too would move more work into the out-projection and fc1 epilogues than it saves.
     uint16_t* o16 = static_cast<uint16_t*>(h->o);
-    rec(0, wenc_host::launch_layernorm(src, P.ln1_w, P.ln1_b, h->xn, M, d, c.ln_eps, 1, s));
-    rec(1, wenc_host::launch_gemm(h->tm_xn, P.tm_wqkv, M, 3 * d, d, h->bn_qkv, WENC_EPI_BIAS_BF16, P.bqkv, nullptr,
-                                  h->qkv, h->err_dev, h->num_sms, s));
+    uint16_t* xn16 = static_cast<uint16_t*>(h->xn);
+    wenc_host::GemmExtra ln1, wr;
+    ln1.colsum = P.cs_qkv;
+    ln1.stats = h->stats;
+    ln1.eps = c.ln_eps;
+    ln1.seg_w = wr.seg_w = h->seg_w;
+    wr.copy = xn16;
+    wr.stats_out = h->stats;
+    rec(1, wenc_host::launch_gemm(h->tm_xn, P.tm_wqkv, M, 3 * d, d, h->bn_qkv, wenc_host::kEpiLnBias, P.bqkv, nullptr,
+                                  h->qkv, h->err_dev, h->num_sms, s, false, 0, ln1));
     rec(2, wenc_host::launch_attention_main(h->tm_q, h->tm_kv, h->tm_kv, 0, d, 2 * d, o16, d, B, T, H, h->err_dev, s,
                                             h->attn_splits, h->part_o, h->part_ml));
     if (wenc_host::attention_launches(T, h->attn_splits) == 2)
@@ -384,8 +402,12 @@ void enqueue_blocks(wenc* h, const float* in, float* out, int B, int first, int 
     rec(0, wenc_host::launch_layernorm(h->x, P.ln2_w, P.ln2_b, h->xn, M, d, c.ln_eps, 1, s));
     rec(4, wenc_host::launch_gemm(h->tm_xn, P.tm_w1, M, f, d, h->bn_1, WENC_EPI_BIAS_GELU_BF16, P.b1, nullptr, h->u,
                                   h->err_dev, h->num_sms, s));
-    rec(5, wenc_host::launch_gemm(h->tm_u, P.tm_w2, M, d, f, h->bn_2, WENC_EPI_BIAS_RESID_F32, P.b2, h->x, dst_final,
-                                  h->err_dev, h->num_sms, s));
+    if (last)  // the call's output: the final LayerNorm (its own kernel) or the caller reads it
+      rec(5, wenc_host::launch_gemm(h->tm_u, P.tm_w2, M, d, f, h->bn_2, WENC_EPI_BIAS_RESID_F32, P.b2, h->x, dst_final,
+                                    h->err_dev, h->num_sms, s));
+    else
+      rec(5, wenc_host::launch_gemm(h->tm_u, P.tm_w2, M, d, f, h->bn_2, wenc_host::kEpiResidStats, P.b2, h->x, dst_final,
+                                    h->err_dev, h->num_sms, s, false, 0, wr));
     src = h->x;
   }
   if (rec.e == cudaSuccess) {
@@ -451,7 +473,7 @@ wenc_status wenc_create(const wenc_config* cfg, const wenc_layer_weights* layers
 
   // ---- weights arena
   Arena wa;
-  struct Off { size_t wqkv, wo, w1, w2, ln1_w, ln1_b, bqkv, bo, ln2_w, ln2_b, b1, b2; };
+  struct Off { size_t wqkv, wo, w1, w2, ln1_w, ln1_b, bqkv, bo, ln2_w, ln2_b, b1, b2, cs_qkv; };
   std::vector<Off> offs(L);
   for (int l = 0; l < L; ++l) {
     Off& o = offs[l];
@@ -463,6 +485,7 @@ wenc_status wenc_create(const wenc_config* cfg, const wenc_layer_weights* layers
     o.bqkv = wa.take(3 * d * 4); o.bo = wa.take(d * 4);
     o.ln2_w = wa.take(d * 4); o.ln2_b = wa.take(d * 4);
     o.b1 = wa.take(f * 4); o.b2 = wa.take(d * 4);
+    if (!h->tf32) o.cs_qkv = wa.take(3 * d * 4);
   }
   const size_t off_lnf_w = wa.take(d * 4), off_lnf_b = wa.take(d * 4);
   cudaError_t e = cudaMalloc(&h->weight_arena, wa.used);
@@ -478,6 +501,10 @@ wenc_status wenc_create(const wenc_config* cfg, const wenc_layer_weights* layers
   Arena ka;
   const size_t off_x = ka.take(rows * d * 4), off_xn = ka.take(rows * d * es), off_qkv = ka.take(rows * 3 * d * es),
                off_o = ka.take(rows * d * es), off_u = ka.take(rows * f * es);
+  // BF16: the per-row segment statistics the LayerNorm-folded GEMMs read (segments of bn / 2
+  // columns, bn the tile width of the GEMMs that write the residual stream)
+  h->seg_w = wenc_host::gemm_pick_bn(d) / 2;
+  const size_t off_stats = h->tf32 ? 0 : ka.take(rows * (d / h->seg_w) * sizeof(float2));
   // Small batches leave most SMs idle in attention: split the keys among more CTAs then (the
   // bf16 kernel only).
   h->attn_splits =
@@ -497,6 +524,7 @@ wenc_status wenc_create(const wenc_config* cfg, const wenc_layer_weights* layers
   h->qkv = kb + off_qkv;
   h->o = kb + off_o;
   h->u = kb + off_u;
+  if (!h->tf32) h->stats = reinterpret_cast<float2*>(kb + off_stats);
   if (h->attn_splits > 1) {
     h->part_o = reinterpret_cast<float*>(kb + off_po);
     h->part_ml = reinterpret_cast<float2*>(kb + off_pml);
@@ -532,22 +560,38 @@ wenc_status wenc_create(const wenc_config* cfg, const wenc_layer_weights* layers
     const size_t dd = size_t(d) * d;
     uint8_t* qkv_w = static_cast<uint8_t*>(P.wqkv);
     const int wdt = cfg->weight_dtype;
-    if (e == cudaSuccess) e = pack_matrix(w.wq, wdt, h->tf32, qkv_w, dd, s);
-    if (e == cudaSuccess) e = pack_matrix(w.wk, wdt, h->tf32, qkv_w + dd * es, dd, s);
-    if (e == cudaSuccess) e = pack_matrix(w.wv, wdt, h->tf32, qkv_w + 2 * dd * es, dd, s);
-    if (e == cudaSuccess) e = pack_matrix(w.wo, wdt, h->tf32, P.wo, dd, s);
-    if (e == cudaSuccess) e = pack_matrix(w.w1, wdt, h->tf32, P.w1, size_t(f) * d, s);
-    if (e == cudaSuccess) e = pack_matrix(w.w2, wdt, h->tf32, P.w2, size_t(d) * f, s);
     auto cp = [&](float* dst, const float* src, size_t n) {
       if (e == cudaSuccess) e = cudaMemcpyAsync(dst, src, n * 4, cudaMemcpyDeviceToDevice, s);
     };
+    if (h->tf32) {
+      if (e == cudaSuccess) e = pack_matrix(w.wq, wdt, h->tf32, qkv_w, dd, s);
+      if (e == cudaSuccess) e = pack_matrix(w.wk, wdt, h->tf32, qkv_w + dd * es, dd, s);
+      if (e == cudaSuccess) e = pack_matrix(w.wv, wdt, h->tf32, qkv_w + 2 * dd * es, dd, s);
+      if (e == cudaSuccess) e = pack_matrix(w.w1, wdt, h->tf32, P.w1, size_t(f) * d, s);
+      cp(P.bqkv, w.bq, d);
+      if (e == cudaSuccess) e = cudaMemsetAsync(P.bqkv + d, 0, size_t(d) * 4, s);  // K has no bias
+      cp(P.bqkv + 2 * d, w.bv, d);
+      cp(P.b1, w.b1, f);
+    } else {
+      // LN1 folded into Q, K, V (K's own bias is absent; its folded bias is Wk ln1_b):
+      // W' = bf16(W diag(ln1_w)), the row sums of W', bias' = W ln1_b + bias
+      P.cs_qkv = reinterpret_cast<float*>(wb + o.cs_qkv);
+      const bool wbf = wdt == WENC_DTYPE_BF16;
+      uint16_t* q16 = reinterpret_cast<uint16_t*>(qkv_w);
+      const void* srcs[3] = {w.wq, w.wk, w.wv};
+      const float* bsrc[3] = {w.bq, nullptr, w.bv};
+      for (int i = 0; i < 3 && e == cudaSuccess; ++i)
+        e = wenc_host::launch_fold_ln(srcs[i], wbf, w.ln1_w, w.ln1_b, bsrc[i], q16 + i * dd, P.cs_qkv + i * d,
+                                      P.bqkv + i * d, d, d, s);
+      if (e == cudaSuccess) e = pack_matrix(w.w1, wdt, false, P.w1, size_t(f) * d, s);
+      cp(P.b1, w.b1, f);
+    }
+    if (e == cudaSuccess) e = pack_matrix(w.wo, wdt, h->tf32, P.wo, dd, s);
+    if (e == cudaSuccess) e = pack_matrix(w.w2, wdt, h->tf32, P.w2, size_t(d) * f, s);
     cp(P.ln1_w, w.ln1_w, d); cp(P.ln1_b, w.ln1_b, d);
-    cp(P.bqkv, w.bq, d);
-    if (e == cudaSuccess) e = cudaMemsetAsync(P.bqkv + d, 0, size_t(d) * 4, s);  // K has no bias
-    cp(P.bqkv + 2 * d, w.bv, d);
     cp(P.bo, w.bo, d);
     cp(P.ln2_w, w.ln2_w, d); cp(P.ln2_b, w.ln2_b, d);
-    cp(P.b1, w.b1, f); cp(P.b2, w.b2, d);
+    cp(P.b2, w.b2, d);
   }
   if (cfg->final_ln && e == cudaSuccess) {
     h->lnf_w = reinterpret_cast<float*>(wb + off_lnf_w);
@@ -603,7 +647,9 @@ int wenc_forward_launches(const wenc* h, int first, int count, int apply_final_l
   if (!h || first < 0 || count < 0 || first + count > h->cfg.n_layers) return -1;
   const bool final_ln = apply_final_ln && h->cfg.final_ln;
   const int attn = h->tf32 ? 1 : wenc_host::attention_launches(h->cfg.seq_len, h->attn_splits);
-  int n = (6 + attn) * count;
+  // TF32: LN1, QKV, attention, out-proj, LN2, fc1, fc2 per block. BF16: LN1 is folded into the
+  // QKV GEMM, plus one row-statistics launch for the first block's input.
+  int n = h->tf32 ? (6 + attn) * count : (5 + attn) * count + (count > 0 ? 1 : 0);
   if (final_ln) n += 1;
   else if (count == 0) n += 1;  // the copy in -> out
   return n;

@@ -98,34 +98,62 @@ __device__ __forceinline__ void load_resid(float4 (&rr)[8], const float* resid, 
   }
 }
 
+// Per-row state of the LayerNorm-related epilogues for the eight rows (4i + lane/8) a lane
+// handles in every chunk of a tile: the folded LayerNorm's mean and 1/std (EPI 5), or the
+// running (mean, M2) of the row segment being written (EPI 7).
+struct RowState {
+  float a[8], b[8];
+};
+
 // EPI 0 = bias, 1 = bias + GELU, 2 = residual + bias (fp32 out), 3 = GELU(bias) + table row
-// (fp32 out), 4 = bias with planar output (plane width `plane`). For EPI 0, 1 and 4 the output
-// is bf16 (F32OUT false) or fp32 rounded to TF32 (F32OUT true: the operand of a TF32 GEMM).
+// (fp32 out), 4 = bias with planar output (plane width `plane`), 5 = LayerNorm folded in
+// (rstd (acc - mean colsum) + bias, bf16 out), 7 = as 2, plus a bf16 copy and the row
+// segment's statistics. For EPI 0, 1 and 4 the output is bf16 (F32OUT false) or fp32 rounded
+// to TF32 (F32OUT true: the operand of a TF32 GEMM). `chunk` is the chunk's index within the
+// warp's column segment (EPI 7 merges the chunk statistics in that order).
 template <int EPI, bool F32OUT>
 __device__ __forceinline__ void epilogue_chunk(const uint32_t (&acc)[32], uint32_t stage, int lane, int grow0, int M,
                                                int N, int col, const float* __restrict__ bias,
-                                               const float4 (&rr)[8], void* out, int plane) {
+                                               const float4 (&rr)[8], void* out, int plane,
+                                               const wenc_host::GemmExtra& ex, RowState& rs, int chunk) {
 #pragma unroll
   for (int q = 0; q < 8; ++q)
     st_shared_v4(stage_addr(stage, lane, q), acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
   __syncwarp();
   const int sub = lane >> 3, cl = lane & 7;
   const float4 bb = __ldg(reinterpret_cast<const float4*>(bias + col) + cl);
+  float4 cs = make_float4(0.f, 0.f, 0.f, 0.f);
+  if constexpr (EPI == 5) cs = __ldg(reinterpret_cast<const float4*>(ex.colsum + col) + cl);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int r = 4 * i + sub;
     const float4 a = ld_shared_f4(stage_addr(stage, r, cl));
     const int grow = grow0 + r;
+    float4 v = make_float4(a.x + bb.x, a.y + bb.y, a.z + bb.z, a.w + bb.w);
+    if constexpr (EPI == 5) {
+      const float mu = rs.a[i], rstd = rs.b[i];
+      v = make_float4(fmaf(rstd, fmaf(-mu, cs.x, a.x), bb.x), fmaf(rstd, fmaf(-mu, cs.y, a.y), bb.y),
+                      fmaf(rstd, fmaf(-mu, cs.z, a.z), bb.z), fmaf(rstd, fmaf(-mu, cs.w, a.w), bb.w));
+    }
+    if constexpr (EPI == 7) {
+      v = make_float4(rr[i].x + v.x, rr[i].y + v.y, rr[i].z + v.z, rr[i].w + v.w);
+      // statistics of this row's 32 columns (8 lanes x 4 values), merged into the segment's
+      // running (mean, M2) in chunk order
+      float cm, cq;
+      chunk_stats32(v, cm, cq);
+      chunk_merge32(rs.a[i], rs.b[i], cm, cq, chunk);
+    }
     if (grow < M) {
       size_t off = static_cast<size_t>(grow) * N + col + 4 * cl;
       if constexpr (EPI == 4) {  // the chunk's 32 columns lie in one plane (plane % 32 == 0)
         const int pl = col / plane;
         off = (static_cast<size_t>(pl) * M + grow) * plane + (col - pl * plane) + 4 * cl;
       }
-      float4 v = make_float4(a.x + bb.x, a.y + bb.y, a.z + bb.z, a.w + bb.w);
-      if constexpr (EPI == 2) {
-        v = make_float4(rr[i].x + v.x, rr[i].y + v.y, rr[i].z + v.z, rr[i].w + v.w);
+      if constexpr (EPI == 2 || EPI == 7) {
+        if constexpr (EPI == 2) v = make_float4(rr[i].x + v.x, rr[i].y + v.y, rr[i].z + v.z, rr[i].w + v.w);
         *reinterpret_cast<float4*>(static_cast<float*>(out) + off) = v;
+        if constexpr (EPI == 7)
+          *reinterpret_cast<uint2*>(ex.copy + off) = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
       } else if constexpr (EPI == 3) {
         v = make_float4(gelu_erf(v.x) + rr[i].x, gelu_erf(v.y) + rr[i].y, gelu_erf(v.z) + rr[i].z,
                         gelu_erf(v.w) + rr[i].w);
@@ -150,7 +178,7 @@ template <int BN, int EPI, bool TF32>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, int M, int N,
                    int K, const float* __restrict__ bias, const float* resid, void* out, uint32_t* err,
-                   int row_period) {
+                   int row_period, const wenc_host::GemmExtra ex) {
   using C = GemmCfg<BN>;
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -297,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto row0_of = [&](int t) { return tile_m(t) * BM + quad * 32; };
     auto col_of = [&](int t) { return tile_n(t) * BN + col_half * (BN / 2); };
     float4 rb[2][8];
-    constexpr bool kRowInput = (EPI == 2 || EPI == 3);  // residual rows or table rows
+    constexpr bool kRowInput = (EPI == 2 || EPI == 3 || EPI == 7);  // residual rows or table rows
     if constexpr (kRowInput) {
       if (blockIdx.x < num_tiles) {
         load_resid(rb[0], resid, row0_of(blockIdx.x), M, N, col_of(blockIdx.x), lane, row_period);
@@ -311,6 +339,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int grow0 = row0_of(tile);
       const int c0 = col_of(tile);
       const int next = tile + gridDim.x;
+      RowState rs;  // (EPI 5: loaded before the accumulator wait, to hide the load latency)
+      if constexpr (EPI == 5) {
+        // The folded LayerNorm's mean and 1/std of this lane's eight rows, from the producer's
+        // segment statistics (equal-width segments: mean of the means, M2 by the parallel rule).
+        // The 8 lanes that share a row split its segments (lane cl takes segments cl + 8 s,
+        // s < 4: up to 32), issue all their loads together, and combine by shuffles in a fixed
+        // order.
+        const int nseg = K / ex.seg_w;
+        const int sub = lane >> 3, cl = lane & 7;
+        float2 sg[8][4];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int grow = min(grow0 + 4 * i + sub, M - 1);
+          const float2* st = ex.stats + static_cast<size_t>(grow) * nseg;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) sg[i][q] = cl + 8 * q < nseg ? st[cl + 8 * q] : make_float2(0.0f, 0.0f);
+        }
+        const float inv_nseg = 1.0f / nseg;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float msum = (sg[i][0].x + sg[i][1].x) + (sg[i][2].x + sg[i][3].x);
+          msum += __shfl_xor_sync(0xffffffffu, msum, 1);
+          msum += __shfl_xor_sync(0xffffffffu, msum, 2);
+          msum += __shfl_xor_sync(0xffffffffu, msum, 4);
+          const float mu = msum * inv_nseg;
+          float m2 = 0.0f;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float dq = sg[i][q].x - mu;
+            if (cl + 8 * q < nseg) m2 += sg[i][q].y + ex.seg_w * dq * dq;
+          }
+          m2 += __shfl_xor_sync(0xffffffffu, m2, 1);
+          m2 += __shfl_xor_sync(0xffffffffu, m2, 2);
+          m2 += __shfl_xor_sync(0xffffffffu, m2, 4);
+          rs.a[i] = mu;
+          rs.b[i] = 1.0f / sqrtf(m2 / K + ex.eps);
+        }
+      }
       if (!mbar_wait_warp(tfull_bar(acc), acc_phase, wc, 4)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN + col_half * (BN / 2);
@@ -324,12 +390,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(tempty_bar(acc));
         }
-        epilogue_chunk<EPI, TF32>(r, stage, lane, grow0, M, N, c0 + c * 32, bias, rb[c & 1], out, row_period);
+        epilogue_chunk<EPI, TF32>(r, stage, lane, grow0, M, N, c0 + c * 32, bias, rb[c & 1], out, row_period, ex, rs,
+                                  c);
         if constexpr (kRowInput) {
           if (c + 2 < CH) {
             load_resid(rb[c & 1], resid, grow0, M, N, c0 + (c + 2) * 32, lane, row_period);
           } else if (next < num_tiles) {
             load_resid(rb[c & 1], resid, row0_of(next), M, N, col_of(next) + (c + 2 - CH) * 32, lane, row_period);
+          }
+        }
+      }
+      if constexpr (EPI == 7) {
+        // this warp's column segment (BN / 2 columns) of its eight rows is complete
+        const int sub = lane >> 3, cl = lane & 7;
+        if (cl == 0) {
+          const int nseg = N / ex.seg_w, seg = c0 / ex.seg_w;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int grow = grow0 + 4 * i + sub;
+            if (grow < M) ex.stats_out[static_cast<size_t>(grow) * nseg + seg] = make_float2(rs.a[i], rs.b[i]);
           }
         }
       }
@@ -347,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int BN, int EPI, bool TF32>
 cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmW, int M, int N, int K, const float* bias,
                        const float* resid, void* out, uint32_t* err, int num_sms, cudaStream_t stream,
-                       int row_period) {
+                       int row_period, const wenc_host::GemmExtra& ex) {
   using C = GemmCfg<BN>;
   auto kern = gemm_tc_kernel<BN, EPI, TF32>;
   static int configured_device = -1;  // attribute is per device; cheap to repeat
@@ -361,7 +440,7 @@ cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmW, int M, in
   const int tiles = ((M + BM - 1) / BM) * (N / BN);
   const int grid = tiles < num_sms ? tiles : num_sms;
   return wenc_host::launch_pdl(kern, dim3(grid), dim3(kThreads), C::SMEM, stream, tmA, tmW, M, N, K, bias, resid, out,
-                               err, row_period);
+                               err, row_period, ex);
 }
 
 }  // namespace
@@ -376,13 +455,17 @@ int gemm_pick_bn(int N) {
 
 cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmW, int M, int N, int K, int bn, int epilogue,
                         const float* bias, const float* resid, void* out, uint32_t* err, int num_sms,
-                        cudaStream_t stream, bool tf32, int row_period) {
+                        cudaStream_t stream, bool tf32, int row_period, const GemmExtra& ex) {
   if (M <= 0) return cudaSuccess;
+  if (epilogue == 5 &&
+      (!ex.colsum || !ex.stats || ex.seg_w <= 0 || K % ex.seg_w != 0 || K / ex.seg_w > 32 || tf32))
+    return cudaErrorInvalidValue;
+  if (epilogue == 7 && (!ex.copy || !ex.stats_out || ex.seg_w != bn / 2 || tf32)) return cudaErrorInvalidValue;
   if (epilogue == 3 && row_period <= 0) return cudaErrorInvalidValue;
   if (epilogue == 4 && (row_period <= 0 || row_period % 32 != 0 || N % row_period != 0)) return cudaErrorInvalidValue;
 #define WENC_GEMM_CASE(BNV, EPIV, TF) \
   if (bn == BNV && epilogue == EPIV && tf32 == TF)                                        \
-    return launch_one<BNV, EPIV, TF>(tmA, tmW, M, N, K, bias, resid, out, err, num_sms, stream, row_period);
+    return launch_one<BNV, EPIV, TF>(tmA, tmW, M, N, K, bias, resid, out, err, num_sms, stream, row_period, ex);
   WENC_GEMM_CASE(256, 0, false)
   WENC_GEMM_CASE(256, 1, false)
   WENC_GEMM_CASE(256, 2, false)
@@ -393,6 +476,10 @@ cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmW, int M, i
   WENC_GEMM_CASE(128, 3, false)
   WENC_GEMM_CASE(256, 4, false)
   WENC_GEMM_CASE(128, 4, false)
+  WENC_GEMM_CASE(256, 5, false)
+  WENC_GEMM_CASE(128, 5, false)
+  WENC_GEMM_CASE(256, 7, false)
+  WENC_GEMM_CASE(128, 7, false)
   WENC_GEMM_CASE(256, 0, true)
   WENC_GEMM_CASE(256, 1, true)
   WENC_GEMM_CASE(256, 2, true)

@@ -52,6 +52,13 @@ bool layernorm_supported(int d);
 cudaError_t launch_layernorm(const float* x, const float* w, const float* b, void* y, int rows, int d, float eps,
                              int out_fmt, cudaStream_t stream);
 
+// Row statistics for a LayerNorm-folded GEMM (see GemmExtra): xb = bf16(x), stats [rows][d / seg]
+// = (mean, M2) of each seg-column segment (seg 128 or 64).
+cudaError_t launch_row_stats(const float* x, uint16_t* xb, float2* stats, int rows, int d, int seg, cudaStream_t stream);
+// Fold a LayerNorm (ln_w, ln_b) into the GEMM after it (see fold_ln_kernel in ln.cu).
+cudaError_t launch_fold_ln(const void* w, bool w_bf16, const float* ln_w, const float* ln_b, const float* bias,
+                           uint16_t* wp, float* colsum, float* bias_out, int n_out, int k, cudaStream_t stream);
+
 // ---------------------------------------------------------------- GEMM (tcgen05)
 // C[M, N] = A[M, K] * W[N, K]^T with a fused epilogue (wenc_epilogue values).
 // Tile: 128 x bn (bn = 256 or 128), k-block 64. tmA: box 64 x 128 over A; tmW: box 64 x bn over W.
@@ -64,12 +71,31 @@ constexpr int kGemmBK = 64;
 // Epilogue 3 (internal, the stem's conv2): out fp32 = GELU_erf(A W^T + bias) + resid[row % row_period]
 // with resid a [row_period, N] fp32 table (row_period > 0).
 constexpr int kEpiGeluTable = 3;
+// LayerNorm folded into the GEMMs around it (the BF16 forward folds LN1 into QKV):
+// - epilogue 5: out bf16 = rstd_r (acc - mu_r colsum_n) + bias_n, where the GEMM
+//   ran on the raw residual stream x (bf16 copy) against W' = W diag(ln_w), colsum = row sums of W'
+//   and bias = W ln_b + b, and (mu_r, rstd_r) come from the per-row segment statistics `stats`
+//   ([M][K / seg_w] float2 = (segment mean, segment M2), each segment seg_w columns wide);
+// - epilogue 7: as epilogue 2 (out fp32 = resid + acc + bias), and also writes `copy`, the output
+//   rounded to bf16, and `stats_out`, the (mean, M2) of every seg_w-column row segment (seg_w =
+//   bn / 2), which the next LN-folded GEMM reads.
+struct GemmExtra {
+  const float* colsum = nullptr;
+  const float2* stats = nullptr;
+  float2* stats_out = nullptr;
+  uint16_t* copy = nullptr;
+  float eps = 0.0f;
+  int seg_w = 0;
+};
+constexpr int kEpiLnBias = 5;
+constexpr int kEpiResidStats = 7;
+
 // Epilogue 4 (internal, the cross K/V precompute): as epilogue 0, written as planes of width
 // row_period: out[(col / P) * M * P + row * P + col % P]. P % 32 == 0 and N % P == 0.
 constexpr int kEpiBiasPlanes = 4;
 cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmW, int M, int N, int K, int bn, int epilogue,
                         const float* bias, const float* resid, void* out, uint32_t* err, int num_sms,
-                        cudaStream_t stream, bool tf32 = false, int row_period = 0);
+                        cudaStream_t stream, bool tf32 = false, int row_period = 0, const GemmExtra& ex = GemmExtra());
 
 // ---------------------------------------------------------------- attention (tcgen05)
 // Q/K/V tiles are read through 3-D maps [B][T][row] (box 64 x 128 elements for all three);

@@ -134,6 +134,97 @@ __global__ void to_tf32_kernel(const void* __restrict__ src, int src_bf16, float
   }
 }
 
+// The statistics a LayerNorm-folded GEMM needs, for a block's input rows (the BF16 forward's
+// first block; later blocks get them from the residual epilogue of the GEMM before): one warp
+// per row writes the row as bf16 (the GEMM operand) and the (mean, M2) of each SEG-column
+// segment, computed exactly as that epilogue does (statistics of 32-column chunks, merged in
+// column order), so the two give the same bits.
+template <int NV, int SEG>
+__global__ void __launch_bounds__(32 * kRowsPerBlock)
+    row_stats_kernel(const float* __restrict__ x, uint16_t* __restrict__ xb, float2* __restrict__ stats, int rows) {
+  constexpr int D = NV * 128;
+  constexpr int CPS = SEG / 32;  // 32-column chunks per segment
+  wenc_dev::pdl_trigger();
+  wenc_dev::pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const float4* xr = reinterpret_cast<const float4*>(x + static_cast<size_t>(row) * D);
+  float4 v[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) v[i] = xr[lane + 32 * i];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    reinterpret_cast<uint2*>(xb + static_cast<size_t>(row) * D)[lane + 32 * i] =
+        make_uint2(wenc_dev::pack_bf16x2(v[i].x, v[i].y), wenc_dev::pack_bf16x2(v[i].z, v[i].w));
+    // columns 128 i + 32 m .. +31 are chunk m, held by lanes 8 m .. 8 m + 7
+    float cm, cq;
+    wenc_dev::chunk_stats32(v[i], cm, cq);
+#pragma unroll
+    for (int sg = 0; sg < 128 / SEG; ++sg) {
+      float mean = 0.0f, m2 = 0.0f;
+#pragma unroll
+      for (int c = 0; c < CPS; ++c) {
+        const int src = 8 * (sg * CPS + c);
+        wenc_dev::chunk_merge32(mean, m2, __shfl_sync(0xffffffffu, cm, src), __shfl_sync(0xffffffffu, cq, src), c);
+      }
+      if (lane == 0) stats[static_cast<size_t>(row) * (D / SEG) + i * (128 / SEG) + sg] = make_float2(mean, m2);
+    }
+  }
+}
+
+template <int NV>
+cudaError_t launch_row_stats_nv(const float* x, uint16_t* xb, float2* stats, int rows, int seg, cudaStream_t stream) {
+  const int grid = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
+  const dim3 block(32 * kRowsPerBlock);
+  if (seg == 128) return wenc_host::launch_pdl(row_stats_kernel<NV, 128>, dim3(grid), block, 0, stream, x, xb, stats, rows);
+  if (seg == 64) return wenc_host::launch_pdl(row_stats_kernel<NV, 64>, dim3(grid), block, 0, stream, x, xb, stats, rows);
+  return cudaErrorInvalidValue;
+}
+
+// LayerNorm folded into the GEMM that follows it, at set-up: one block per output row n of
+// W [n_out, k] (fp32 or bf16), with the LayerNorm's weight ln_w and shift ln_b [k]:
+//   wp[n, j] = bf16(W[n, j] ln_w[j])           the GEMM's operand
+//   colsum[n] = sum_j wp[n, j]                  (of the rounded values the GEMM multiplies)
+//   bias_out[n] = sum_j W[n, j] ln_b[j] + bias[n]   (bias may be NULL: zero)
+// so that LN(x) W^T + bias = rstd (x wp^T - mean colsum) + bias_out.
+__global__ void __launch_bounds__(256) fold_ln_kernel(const void* __restrict__ w, int w_bf16, const float* __restrict__ ln_w,
+                                                      const float* __restrict__ ln_b, const float* __restrict__ bias,
+                                                      uint16_t* __restrict__ wp, float* __restrict__ colsum,
+                                                      float* __restrict__ bias_out, int k) {
+  const size_t n = blockIdx.x;
+  float s = 0.0f, c = 0.0f;
+  for (int j = threadIdx.x; j < k; j += blockDim.x) {
+    const size_t idx = n * k + j;
+    const float wv = w_bf16 ? __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t*>(w)[idx]) << 16)
+                            : static_cast<const float*>(w)[idx];
+    const __nv_bfloat16 hv = __float2bfloat16_rn(wv * ln_w[j]);  // nearest, ties to even
+    wp[idx] = *reinterpret_cast<const uint16_t*>(&hv);
+    s += __bfloat162float(hv);
+    c = fmaf(wv, ln_b[j], c);
+  }
+  __shared__ float red[2][8];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    s += __shfl_xor_sync(0xffffffffu, s, o);
+    c += __shfl_xor_sync(0xffffffffu, c, o);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    red[0][threadIdx.x >> 5] = s;
+    red[1][threadIdx.x >> 5] = c;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float ts = 0.0f, tc = 0.0f;
+    for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) {
+      ts += red[0][i];
+      tc += red[1][i];
+    }
+    colsum[n] = ts;
+    bias_out[n] = tc + (bias ? bias[n] : 0.0f);
+  }
+}
+
 }  // namespace
 
 namespace wenc_host {
@@ -153,6 +244,26 @@ cudaError_t launch_layernorm(const float* x, const float* w, const float* b, voi
 #undef WENC_LN_CASE
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_row_stats(const float* x, uint16_t* xb, float2* stats, int rows, int d, int seg, cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  switch (d / 128) {
+#define WENC_RS_CASE(N) \
+  case N: return launch_row_stats_nv<N>(x, xb, stats, rows, seg, stream);
+    WENC_RS_CASE(1) WENC_RS_CASE(2) WENC_RS_CASE(3) WENC_RS_CASE(4) WENC_RS_CASE(5) WENC_RS_CASE(6)
+    WENC_RS_CASE(7) WENC_RS_CASE(8) WENC_RS_CASE(9) WENC_RS_CASE(10) WENC_RS_CASE(11) WENC_RS_CASE(12)
+    WENC_RS_CASE(13) WENC_RS_CASE(14) WENC_RS_CASE(15) WENC_RS_CASE(16)
+#undef WENC_RS_CASE
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_fold_ln(const void* w, bool w_bf16, const float* ln_w, const float* ln_b, const float* bias,
+                           uint16_t* wp, float* colsum, float* bias_out, int n_out, int k, cudaStream_t stream) {
+  if (n_out <= 0) return cudaSuccess;
+  fold_ln_kernel<<<n_out, 256, 0, stream>>>(w, w_bf16 ? 1 : 0, ln_w, ln_b, bias, wp, colsum, bias_out, k);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_f32_to_bf16(const float* src, uint16_t* dst, size_t n, cudaStream_t stream) {

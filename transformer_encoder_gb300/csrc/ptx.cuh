@@ -255,6 +255,40 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// ------------------------------------------------------------------ row statistics
+// Mean and M2 (sum of squared deviations) of 32 values held four per lane by the 8 lanes of an
+// aligned lane group (lane & 7 = position of the lane's four values). Two passes; every
+// operation explicitly rounded, so two kernels that call this on the same values get the same
+// bits (the GEMM epilogue that writes the residual stream and the row-statistics kernel).
+__device__ __forceinline__ void chunk_stats32(float4 v, float& mean, float& m2) {
+  float sm = __fadd_rn(__fadd_rn(v.x, v.y), __fadd_rn(v.z, v.w));
+  sm = __fadd_rn(sm, __shfl_xor_sync(0xffffffffu, sm, 1));
+  sm = __fadd_rn(sm, __shfl_xor_sync(0xffffffffu, sm, 2));
+  sm = __fadd_rn(sm, __shfl_xor_sync(0xffffffffu, sm, 4));
+  mean = __fmul_rn(sm, 1.0f / 32.0f);
+  const float dx = __fsub_rn(v.x, mean), dy = __fsub_rn(v.y, mean), dz = __fsub_rn(v.z, mean),
+              dw = __fsub_rn(v.w, mean);
+  float q = __fadd_rn(__fadd_rn(__fmul_rn(dx, dx), __fmul_rn(dy, dy)), __fadd_rn(__fmul_rn(dz, dz), __fmul_rn(dw, dw)));
+  q = __fadd_rn(q, __shfl_xor_sync(0xffffffffu, q, 1));
+  q = __fadd_rn(q, __shfl_xor_sync(0xffffffffu, q, 2));
+  q = __fadd_rn(q, __shfl_xor_sync(0xffffffffu, q, 4));
+  m2 = q;
+}
+
+// Merge the statistics (cm, cq) of chunk c (32 values) into those of chunks 0 .. c-1 (the
+// pairwise update of Chan, Golub and LeVeque for combining sample means and M2).
+__device__ __forceinline__ void chunk_merge32(float& mean, float& m2, float cm, float cq, int c) {
+  if (c == 0) {
+    mean = cm;
+    m2 = cq;
+    return;
+  }
+  const float na = 32.0f * c, nt = __fadd_rn(na, 32.0f);
+  const float delta = __fsub_rn(cm, mean);
+  mean = __fadd_rn(mean, __fmul_rn(delta, __fdiv_rn(32.0f, nt)));
+  m2 = __fadd_rn(__fadd_rn(m2, cq), __fmul_rn(__fmul_rn(delta, delta), __fdiv_rn(__fmul_rn(na, 32.0f), nt)));
+}
+
 // ------------------------------------------------------------------ math helpers
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;

@@ -25,7 +25,7 @@ PREC_BF16, PREC_TF32 = 0, 1
 _STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "OOM", 4: "CUDA", 5: "DEVICE_TIMEOUT"}
 LAUNCH_KINDS = {0: "layernorm", 1: "gemm_qkv", 2: "attention", 3: "gemm_out", 4: "gemm_fc1", 5: "gemm_fc2",
                 6: "layernorm_final", 7: "copy", 8: "attention_combine", 9: "stem_unfold", 10: "gemm_conv1",
-                11: "gemm_conv2", 12: "cross_kv_cast", 13: "gemm_cross_kv"}
+                11: "gemm_conv2", 12: "cross_kv_cast", 13: "gemm_cross_kv", 14: "row_stats"}
 
 EXPORTED_SYMBOLS = (
     "wenc_create", "wenc_forward", "wenc_forward_layers", "wenc_forward_launches", "wenc_set_launch_events",
