@@ -76,6 +76,9 @@ WORKLOADS = {
     # One block at large-v3 dims and batch 16: every kernel launch has exactly the shape it has
     # inside the 32-block stack, with ~1 GB on the device (used for profiler captures).
     "large_block": Workload("large_block", 16, 1280, 20, 5120, 1, final_ln=True, bf16_weights=True, n_mels=128),
+    # Two such blocks: the first block's fc2 also writes the row statistics and bf16 copy the
+    # second block's QKV reads, as every block but the last does in the 32-block stack.
+    "large_pair": Workload("large_pair", 16, 1280, 20, 5120, 2, final_ln=True, bf16_weights=True, n_mels=128),
 }
 
 
