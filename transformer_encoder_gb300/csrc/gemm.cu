@@ -67,6 +67,29 @@ __device__ __forceinline__ float gelu_erf(float z) {
   return 0.5f * z * (1.0f + copysignf(erf_abs, z));
 }
 
+// The same GELU on two values at once: the polynomial and the products run as packed fp32x2
+// operations (one instruction per pair), the reciprocal and the exponential per value.
+__device__ __forceinline__ void gelu_erf_x2(float& z0, float& z1) {
+  const float x0 = fabsf(z0) * 0.70710678118654752f, x1 = fabsf(z1) * 0.70710678118654752f;
+  float t0, t1;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t0) : "f"(fmaf(0.3275911f, x0, 1.0f)));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t1) : "f"(fmaf(0.3275911f, x1, 1.0f)));
+  const uint64_t t = pack_f32x2(t0, t1);
+  uint64_t poly = fma_f32x2(t, pack_f32x2(1.061405429f, 1.061405429f), pack_f32x2(-1.453152027f, -1.453152027f));
+  poly = fma_f32x2(t, poly, pack_f32x2(1.421413741f, 1.421413741f));
+  poly = fma_f32x2(t, poly, pack_f32x2(-0.284496736f, -0.284496736f));
+  poly = fma_f32x2(t, poly, pack_f32x2(0.254829592f, 0.254829592f));
+  poly = mul_f32x2(poly, t);
+  const uint64_t xx = pack_f32x2(x0, x1);
+  float a0, a1;
+  unpack_f32x2(mul_f32x2(mul_f32x2(xx, xx), pack_f32x2(-1.4426950408889634f, -1.4426950408889634f)), a0, a1);
+  const uint64_t neg_e = pack_f32x2(-ex2_approx(a0), -ex2_approx(a1));  // -exp(-x^2)
+  float r0, r1;
+  unpack_f32x2(fma_f32x2(poly, neg_e, pack_f32x2(1.0f, 1.0f)), r0, r1);  // erf(|x|)
+  const uint64_t one_p = pack_f32x2(1.0f + copysignf(r0, z0), 1.0f + copysignf(r1, z1));  // 1 + erf(x)
+  unpack_f32x2(mul_f32x2(mul_f32x2(pack_f32x2(z0, z1), pack_f32x2(0.5f, 0.5f)), one_p), z0, z1);
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
@@ -155,12 +178,14 @@ __device__ __forceinline__ void epilogue_chunk(const uint32_t (&acc)[32], uint32
         if constexpr (EPI == 7)
           *reinterpret_cast<uint2*>(ex.copy + off) = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
       } else if constexpr (EPI == 3) {
-        v = make_float4(gelu_erf(v.x) + rr[i].x, gelu_erf(v.y) + rr[i].y, gelu_erf(v.z) + rr[i].z,
-                        gelu_erf(v.w) + rr[i].w);
+        gelu_erf_x2(v.x, v.y);
+        gelu_erf_x2(v.z, v.w);
+        v = make_float4(v.x + rr[i].x, v.y + rr[i].y, v.z + rr[i].z, v.w + rr[i].w);
         *reinterpret_cast<float4*>(static_cast<float*>(out) + off) = v;
       } else {
         if constexpr (EPI == 1) {
-          v.x = gelu_erf(v.x); v.y = gelu_erf(v.y); v.z = gelu_erf(v.z); v.w = gelu_erf(v.w);
+          gelu_erf_x2(v.x, v.y);
+          gelu_erf_x2(v.z, v.w);
         }
         if constexpr (F32OUT)
           *reinterpret_cast<float4*>(static_cast<float*>(out) + off) =
