@@ -52,23 +52,9 @@ struct GemmCfg {
 // approximation of Abramowitz & Stegun, Handbook of Mathematical Functions, formula 7.1.26:
 //   erf(x) = 1 - (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-x^2),  t = 1 / (1 + p x),  x >= 0,
 // |error| <= 1.5e-7, far below the bf16 rounding (2^-9 relative) of the fc1 output it feeds.
-// erf is odd, so erf(-x) = -erf(x). Two MUFU operations (reciprocal, exp2) and a handful of FMAs.
-__device__ __forceinline__ float gelu_erf(float z) {
-  const float x = fabsf(z) * 0.70710678118654752f;
-  float t;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t) : "f"(fmaf(0.3275911f, x, 1.0f)));
-  float poly = fmaf(t, 1.061405429f, -1.453152027f);
-  poly = fmaf(t, poly, 1.421413741f);
-  poly = fmaf(t, poly, -0.284496736f);
-  poly = fmaf(t, poly, 0.254829592f);
-  poly *= t;
-  const float e = ex2_approx(-1.4426950408889634f * x * x);  // exp(-x^2)
-  const float erf_abs = fmaf(-poly, e, 1.0f);
-  return 0.5f * z * (1.0f + copysignf(erf_abs, z));
-}
-
-// The same GELU on two values at once: the polynomial and the products run as packed fp32x2
-// operations (one instruction per pair), the reciprocal and the exponential per value.
+// erf is odd, so erf(-x) = -erf(x). Two MUFU operations (reciprocal, exp2) per value; evaluated
+// on two values at once, the polynomial and the products as packed fp32x2 operations (one
+// instruction per pair).
 __device__ __forceinline__ void gelu_erf_x2(float& z0, float& z1) {
   const float x0 = fabsf(z0) * 0.70710678118654752f, x1 = fabsf(z1) * 0.70710678118654752f;
   float t0, t1;
