@@ -146,6 +146,27 @@ def test_forward_in_place_and_partial_batch():
     assert torch.equal(enc.forward(_t(x)), ref)  # deterministic
 
 
+@pytest.mark.parametrize("precision", ["bf16", "tf32"])
+def test_windows_independent_of_batch_large_dims(precision):
+    """A window's output is the same bits whatever batch it runs in, at large-v3 dims (two blocks).
+
+    The GEMMs cut a last partial wave into half-width units: at B = 1 every out-projection and fc2
+    tile runs as two M128 N128 products, at B = 16 window 0's rows are whole 128 x 256 tiles; each
+    output element must still be the same fixed-order dot product (no split of K, no batch-sized
+    reduction)."""
+    import torch
+    w = synth.WORKLOADS["large_pair"]
+    enc, _, _, rng = make_encoder(w, keep_host_layers=False, precision=precision)
+    x = synth.make_input(w, rng)
+    full = enc.forward(_t(x))
+    first = enc.forward(_t(x[:1]))
+    last = enc.forward(_t(x[-1:]))
+    torch.cuda.synchronize()
+    enc.sync_status()
+    assert torch.equal(first[0], full[0])
+    assert torch.equal(last[0], full[-1])
+
+
 def test_argument_errors():
     import torch
     from transformer_encoder_gb300 import WencError

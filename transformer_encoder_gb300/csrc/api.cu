@@ -202,6 +202,7 @@ struct wenc {
     // holds the row sums of the folded matrix; null for TF32
     float* cs_qkv = nullptr;
     CUtensorMap tm_wqkv, tm_wo, tm_w1, tm_w2;
+    CUtensorMap tm_wqkv_h, tm_wo_h, tm_w1_h, tm_w2_h;  // the same with half-height boxes
   };
   std::vector<Layer> layers;
   float* lnf_w = nullptr;
@@ -230,13 +231,13 @@ struct wenc {
   void *wc1 = nullptr, *wc2 = nullptr;  // [d, kp1], [d, 3d] in the operand format
   float *cb1 = nullptr, *cb2 = nullptr, *pos = nullptr;
   void *a1 = nullptr, *h1 = nullptr, *a2 = nullptr;  // unfolded mel, conv1 output, unfolded conv1 output
-  CUtensorMap tm_a1, tm_wc1, tm_a2, tm_wc2;
+  CUtensorMap tm_a1, tm_wc1, tm_a2, tm_wc2, tm_wc1_h, tm_wc2_h;
   // decoder cross K/V weights (wenc_set_cross_kv): [2 n_dec d, d] operand format, bias [2 n_dec d]
   int n_dec = 0, bn_cross = 0;
   void* cross_arena = nullptr;
   void* wx = nullptr;
   float* bx = nullptr;
-  CUtensorMap tm_wx;
+  CUtensorMap tm_wx, tm_wx_h;
 };
 
 namespace {
@@ -342,10 +343,12 @@ void enqueue_stem(wenc* h, const float* mel, float* x, int B, LaunchRec& rec) {
   const int d = c.d_model, T = c.seq_len;
   rec(9, wenc_host::launch_unfold3(mel, true, h->a1, h->tf32, B, 2 * T, h->n_mels, 1, h->kp1, rec.s));
   rec(10, wenc_host::launch_gemm(h->tm_a1, h->tm_wc1, B * 2 * T, d, h->kp1, h->bn_stem, WENC_EPI_BIAS_GELU_BF16,
-                                 h->cb1, nullptr, h->h1, h->err_dev, h->num_sms, rec.s, h->tf32));
+                                 h->cb1, nullptr, h->h1, h->err_dev, h->num_sms, rec.s, h->tf32, 0,
+                                 wenc_host::GemmExtra(), &h->tm_wc1_h));
   rec(9, wenc_host::launch_unfold3(h->h1, h->tf32, h->a2, h->tf32, B, 2 * T, d, 2, 3 * d, rec.s));
   rec(11, wenc_host::launch_gemm(h->tm_a2, h->tm_wc2, B * T, d, 3 * d, h->bn_stem, wenc_host::kEpiGeluTable, h->cb2,
-                                 h->pos, x, h->err_dev, h->num_sms, rec.s, h->tf32, T));
+                                 h->pos, x, h->err_dev, h->num_sms, rec.s, h->tf32, T,
+                                 wenc_host::GemmExtra(), &h->tm_wc2_h));
 }
 
 // The blocks first .. first+count-1 and, if final_ln, the final LayerNorm: in -> out.
@@ -365,16 +368,16 @@ void enqueue_blocks(wenc* h, const float* in, float* out, int B, int first, int 
       // TF32: every GEMM operand is fp32 rounded to TF32 by its producer.
       rec(0, wenc_host::launch_layernorm(src, P.ln1_w, P.ln1_b, h->xn, M, d, c.ln_eps, 2, s));
       rec(1, wenc_host::launch_gemm(h->tm_xn, P.tm_wqkv, M, 3 * d, d, h->bn_qkv, WENC_EPI_BIAS_BF16, P.bqkv, nullptr,
-                                    h->qkv, h->err_dev, h->num_sms, s, true));
+                                    h->qkv, h->err_dev, h->num_sms, s, true, 0, {}, &P.tm_wqkv_h));
       rec(2, wenc_host::launch_attention_tf32(h->tm_q, h->tm_kv, h->tm_kv, 0, d, 2 * d, static_cast<float*>(h->o), d,
                                               B, T, H, h->err_dev, s));
       rec(3, wenc_host::launch_gemm(h->tm_o, P.tm_wo, M, d, d, h->bn_o, WENC_EPI_BIAS_RESID_F32, P.bo, src, h->x,
-                                    h->err_dev, h->num_sms, s, true));
+                                    h->err_dev, h->num_sms, s, true, 0, {}, &P.tm_wo_h));
       rec(0, wenc_host::launch_layernorm(h->x, P.ln2_w, P.ln2_b, h->xn, M, d, c.ln_eps, 2, s));
       rec(4, wenc_host::launch_gemm(h->tm_xn, P.tm_w1, M, f, d, h->bn_1, WENC_EPI_BIAS_GELU_BF16, P.b1, nullptr, h->u,
-                                    h->err_dev, h->num_sms, s, true));
+                                    h->err_dev, h->num_sms, s, true, 0, {}, &P.tm_w1_h));
       rec(5, wenc_host::launch_gemm(h->tm_u, P.tm_w2, M, d, f, h->bn_2, WENC_EPI_BIAS_RESID_F32, P.b2, h->x, dst_final,
-                                    h->err_dev, h->num_sms, s, true));
+                                    h->err_dev, h->num_sms, s, true, 0, {}, &P.tm_w2_h));
       src = h->x;
       continue;
     }
@@ -392,22 +395,22 @@ void enqueue_blocks(wenc* h, const float* in, float* out, int B, int first, int 
     wr.copy = xn16;
     wr.stats_out = h->stats;
     rec(1, wenc_host::launch_gemm(h->tm_xn, P.tm_wqkv, M, 3 * d, d, h->bn_qkv, wenc_host::kEpiLnBias, P.bqkv, nullptr,
-                                  h->qkv, h->err_dev, h->num_sms, s, false, 0, ln1));
+                                  h->qkv, h->err_dev, h->num_sms, s, false, 0, ln1, &P.tm_wqkv_h));
     rec(2, wenc_host::launch_attention_main(h->tm_q, h->tm_kv, h->tm_kv, 0, d, 2 * d, o16, d, B, T, H, h->err_dev, s,
                                             h->attn_splits, h->part_o, h->part_ml));
     if (wenc_host::attention_launches(T, h->attn_splits) == 2)
       rec(8, wenc_host::launch_attention_combine(h->part_o, h->part_ml, o16, d, B, T, H, h->attn_splits, s));
     rec(3, wenc_host::launch_gemm(h->tm_o, P.tm_wo, M, d, d, h->bn_o, WENC_EPI_BIAS_RESID_F32, P.bo, src, h->x,
-                                  h->err_dev, h->num_sms, s));
+                                  h->err_dev, h->num_sms, s, false, 0, {}, &P.tm_wo_h));
     rec(0, wenc_host::launch_layernorm(h->x, P.ln2_w, P.ln2_b, h->xn, M, d, c.ln_eps, 1, s));
     rec(4, wenc_host::launch_gemm(h->tm_xn, P.tm_w1, M, f, d, h->bn_1, WENC_EPI_BIAS_GELU_BF16, P.b1, nullptr, h->u,
-                                  h->err_dev, h->num_sms, s));
+                                  h->err_dev, h->num_sms, s, false, 0, {}, &P.tm_w1_h));
     if (last)  // the call's output: the final LayerNorm (its own kernel) or the caller reads it
       rec(5, wenc_host::launch_gemm(h->tm_u, P.tm_w2, M, d, f, h->bn_2, WENC_EPI_BIAS_RESID_F32, P.b2, h->x, dst_final,
-                                    h->err_dev, h->num_sms, s));
+                                    h->err_dev, h->num_sms, s, false, 0, {}, &P.tm_w2_h));
     else
       rec(5, wenc_host::launch_gemm(h->tm_u, P.tm_w2, M, d, f, h->bn_2, wenc_host::kEpiResidStats, P.b2, h->x, dst_final,
-                                    h->err_dev, h->num_sms, s, false, 0, wr));
+                                    h->err_dev, h->num_sms, s, false, 0, wr, &P.tm_w2_h));
     src = h->x;
   }
   if (rec.e == cudaSuccess) {
@@ -619,6 +622,10 @@ wenc_status wenc_create(const wenc_config* cfg, const wenc_layer_weights* layers
     map2(&P.tm_wo, P.wo, d, d, h->bn_o);
     map2(&P.tm_w1, P.w1, d, f, h->bn_1);
     map2(&P.tm_w2, P.w2, f, d, h->bn_2);
+    map2(&P.tm_wqkv_h, P.wqkv, d, 3 * d, h->bn_qkv / 2);
+    map2(&P.tm_wo_h, P.wo, d, d, h->bn_o / 2);
+    map2(&P.tm_w1_h, P.w1, d, f, h->bn_1 / 2);
+    map2(&P.tm_w2_h, P.w2, f, d, h->bn_2 / 2);
   }
   map2(&h->tm_xn, h->xn, d, rows, wenc_host::kGemmBM);
   map2(&h->tm_o, h->o, d, rows, wenc_host::kGemmBM);
@@ -751,6 +758,8 @@ wenc_status wenc_set_stem(wenc* h, const wenc_stem_weights* w, wenc_stream_t str
   map2(&h->tm_wc1, h->wc1, kp1, d, h->bn_stem);
   map2(&h->tm_a2, h->a2, 3 * d, rows2, wenc_host::kGemmBM);
   map2(&h->tm_wc2, h->wc2, 3 * d, d, h->bn_stem);
+  map2(&h->tm_wc1_h, h->wc1, kp1, d, h->bn_stem / 2);
+  map2(&h->tm_wc2_h, h->wc2, 3 * d, d, h->bn_stem / 2);
   if (!ok) return fail(WENC_ERR_CUDA, "%s", why.c_str());
   h->has_stem = true;
   return WENC_OK;
@@ -833,8 +842,11 @@ wenc_status wenc_set_cross_kv(wenc* h, int n_dec, const void* const* wk, const v
   if (e != cudaSuccess) return cuda_fail(e, "packing the cross K/V weights");
   h->bn_cross = wenc_host::gemm_pick_bn(static_cast<int>(n_out));
   std::string why;
-  const bool ok = h->tf32 ? wenc_host::make_tmap_2d_f32(&h->tm_wx, h->wx, d, n_out, size_t(d) * 4, 32, h->bn_cross, &why)
-                          : wenc_host::make_tmap_2d_bf16(&h->tm_wx, h->wx, d, n_out, size_t(d) * 2, 64, h->bn_cross, &why);
+  const bool ok =
+      h->tf32 ? (wenc_host::make_tmap_2d_f32(&h->tm_wx, h->wx, d, n_out, size_t(d) * 4, 32, h->bn_cross, &why) &&
+                 wenc_host::make_tmap_2d_f32(&h->tm_wx_h, h->wx, d, n_out, size_t(d) * 4, 32, h->bn_cross / 2, &why))
+              : (wenc_host::make_tmap_2d_bf16(&h->tm_wx, h->wx, d, n_out, size_t(d) * 2, 64, h->bn_cross, &why) &&
+                 wenc_host::make_tmap_2d_bf16(&h->tm_wx_h, h->wx, d, n_out, size_t(d) * 2, 64, h->bn_cross / 2, &why));
   if (!ok) return fail(WENC_ERR_CUDA, "%s", why.c_str());
   h->n_dec = n_dec;
   return WENC_OK;
@@ -853,7 +865,8 @@ wenc_status wenc_cross_kv(wenc* h, const float* enc_out, void* kv_out, int B, we
   rec(12, h->tf32 ? wenc_host::launch_to_tf32(enc_out, false, static_cast<float*>(h->xn), n, rec.s)
                   : wenc_host::launch_f32_to_bf16(enc_out, static_cast<uint16_t*>(h->xn), n, rec.s));
   rec(13, wenc_host::launch_gemm(h->tm_xn, h->tm_wx, M, 2 * h->n_dec * d, d, h->bn_cross, wenc_host::kEpiBiasPlanes,
-                                 h->bx, nullptr, kv_out, h->err_dev, h->num_sms, rec.s, h->tf32, d));
+                                 h->bx, nullptr, kv_out, h->err_dev, h->num_sms, rec.s, h->tf32, d,
+                                 wenc_host::GemmExtra(), &h->tm_wx_h));
   if (rec.e != cudaSuccess) return cuda_fail(rec.e, "cross K/V launch");
   return WENC_OK;
 }

@@ -187,9 +187,10 @@ __device__ __forceinline__ void epilogue_chunk(const uint32_t (&acc)[32], uint32
 
 template <int BN, int EPI, bool TF32>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, int M, int N,
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
+                   const __grid_constant__ CUtensorMap tmWh, int half_box, int M, int N,
                    int K, const float* __restrict__ bias, const float* resid, void* out, uint32_t* err,
-                   int row_period, const wenc_host::GemmExtra ex) {
+                   int row_period, const wenc_host::GemmExtra ex, int tail_halves) {
   using C = GemmCfg<BN>;
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -234,6 +235,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   constexpr int BKE = TF32 ? 32 : BK;  // K elements per stage (128-byte rows)
   const int k_blocks = K / BKE;
+  // Work items of this CTA, the same sequence for every role: whole tiles blockIdx.x + i G
+  // (G = gridDim.x) over the first n_dp tiles; then, when the launch splits its last partial
+  // wave (tail_halves), one half-width unit: the n_tail = num_tiles % G remaining tiles become
+  // 2 n_tail units of BN / 2 columns (an M128 N(BN/2) product over the whole K), unit
+  // u = blockIdx.x < 2 n_tail taking half u % 2 of tile n_dp + u / 2. Each output element is
+  // the same fixed-order dot product either way.
+  const int n_tail = tail_halves ? num_tiles % static_cast<int>(gridDim.x) : 0;
+  const int n_dp = num_tiles - n_tail;
+  const int n_mine = (static_cast<int>(blockIdx.x) < n_dp)
+                         ? (n_dp - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
+                         : 0;
+  const bool has_unit = static_cast<int>(blockIdx.x) < 2 * n_tail;
+  // item i of this CTA: its tile and, for the half-width unit, which half (-1: the whole tile)
+  auto item = [&](int i, int& tile, int& half) -> bool {
+    if (i < n_mine) {
+      tile = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
+      half = -1;
+      return true;
+    }
+    if (i == n_mine && has_unit) {
+      tile = n_dp + static_cast<int>(blockIdx.x) / 2;
+      half = static_cast<int>(blockIdx.x) % 2;
+      return true;
+    }
+    return false;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -249,6 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmW);
+    if (half_box) tma_prefetch_desc(&tmWh);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -267,14 +295,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0;
     uint32_t issued_mask = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+    int tile, half;
+    for (int i = 0; ok && item(i, tile, half); ++i) {
       const int m0 = tile_m(tile) * BM;
-      const int n0 = tile_n(tile) * BN;
+      // a half-width unit loads BN / 2 rows of W through the half-box map (or, without one, the
+      // BN rows from its half's first column, rows past N reading as zeros) and multiplies the
+      // first BN / 2 of them
+      const int n0 = tile_n(tile) * BN + (half > 0 ? BN / 2 : 0);
+      const bool hb = half >= 0 && half_box;
+      const uint32_t stage_bytes = hb ? C::A_BYTES + C::B_BYTES / 2 : C::STAGE_BYTES;
       for (int kb = 0; kb < k_blocks; ++kb) {
         if (!mbar_wait(empty_bar(stage), phase ^ 1u, wc, 1)) { ok = false; break; }
-        mbar_arrive_expect_tx(full_bar(stage), C::STAGE_BYTES);
+        mbar_arrive_expect_tx(full_bar(stage), stage_bytes);
         tma_load_2d(sA + stage * C::A_BYTES, &tmA, full_bar(stage), kb * BKE, m0);
-        tma_load_2d(sB + stage * C::B_BYTES, &tmW, full_bar(stage), kb * BKE, n0);
+        tma_load_2d(sB + stage * C::B_BYTES, hb ? &tmWh : &tmW, full_bar(stage), kb * BKE, n0);
         issued_mask |= 1u << stage;
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
@@ -290,12 +324,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1 && lane == 0) {
     // ---------------- UMMA issuer
     // Four MMAs per stage, each over 32 bytes of K (16 bf16 or 8 TF32 elements).
-    constexpr uint32_t idesc = TF32 ? idesc_tf32_f32(BM, BN) : idesc_bf16_f32(BM, BN, false);
+    constexpr uint32_t idesc_full = TF32 ? idesc_tf32_f32(BM, BN) : idesc_bf16_f32(BM, BN, false);
+    constexpr uint32_t idesc_half = TF32 ? idesc_tf32_f32(BM, BN / 2) : idesc_bf16_f32(BM, BN / 2, false);
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    int local = 0;
-    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++local) {
+    int tile, half;
+    for (int local = 0; ok && item(local, tile, half); ++local) {
+      const uint32_t idesc = half < 0 ? idesc_full : idesc_half;
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, wc, 2)) break;
@@ -337,19 +373,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto col_of = [&](int t) { return tile_n(t) * BN + col_half * (BN / 2); };
     float4 rb[2][8];
     constexpr bool kRowInput = (EPI == 2 || EPI == 3 || EPI == 7);  // residual rows or table rows
+    // A half-width unit's BN / 2 columns sit in TMEM columns [0, BN / 2) and belong to the warps
+    // of the first column half; the other warps only release the buffer.
+    auto cols_of = [&](int t, int hf) { return hf < 0 ? col_of(t) : tile_n(t) * BN + hf * (BN / 2); };
+    auto active = [&](int hf) { return hf < 0 || col_half == 0; };
+    int tile, half;
     if constexpr (kRowInput) {
-      if (blockIdx.x < num_tiles) {
-        load_resid(rb[0], resid, row0_of(blockIdx.x), M, N, col_of(blockIdx.x), lane, row_period);
-        if (CH > 1) load_resid(rb[1], resid, row0_of(blockIdx.x), M, N, col_of(blockIdx.x) + 32, lane, row_period);
+      if (item(0, tile, half) && active(half)) {
+        load_resid(rb[0], resid, row0_of(tile), M, N, cols_of(tile, half), lane, row_period);
+        if (CH > 1) load_resid(rb[1], resid, row0_of(tile), M, N, cols_of(tile, half) + 32, lane, row_period);
       }
     }
-    int local = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+    for (int local = 0; item(local, tile, half); ++local) {
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       const int grow0 = row0_of(tile);
-      const int c0 = col_of(tile);
-      const int next = tile + gridDim.x;
+      const int c0 = cols_of(tile, half);
+      int next, next_half;
+      const bool prefetch_next = item(local + 1, next, next_half) && active(next_half);
       RowState rs;  // (EPI 5: loaded before the accumulator wait, to hide the load latency)
       if constexpr (EPI == 5) {
         // The folded LayerNorm's mean and 1/std of this lane's eight rows, from the producer's
@@ -390,7 +431,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!mbar_wait_warp(tfull_bar(acc), acc_phase, wc, 4)) break;
       tc_fence_after();
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN + col_half * (BN / 2);
+      if (!active(half)) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar(acc));
+        continue;
+      }
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN +
+                             (half < 0 ? col_half * (BN / 2) : 0);
 #pragma unroll
       for (int c = 0; c < CH; ++c) {
         uint32_t r[32];
@@ -406,8 +454,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (kRowInput) {
           if (c + 2 < CH) {
             load_resid(rb[c & 1], resid, grow0, M, N, c0 + (c + 2) * 32, lane, row_period);
-          } else if (next < num_tiles) {
-            load_resid(rb[c & 1], resid, row0_of(next), M, N, col_of(next) + (c + 2 - CH) * 32, lane, row_period);
+          } else if (prefetch_next) {
+            load_resid(rb[c & 1], resid, row0_of(next), M, N, cols_of(next, next_half) + (c + 2 - CH) * 32, lane,
+                       row_period);
           }
         }
       }
@@ -435,9 +484,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int BN, int EPI, bool TF32>
-cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmW, int M, int N, int K, const float* bias,
-                       const float* resid, void* out, uint32_t* err, int num_sms, cudaStream_t stream,
-                       int row_period, const wenc_host::GemmExtra& ex) {
+cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmW, const CUtensorMap* tmW_half, int M, int N,
+                       int K, const float* bias, const float* resid, void* out, uint32_t* err, int num_sms,
+                       cudaStream_t stream, int row_period, const wenc_host::GemmExtra& ex) {
   using C = GemmCfg<BN>;
   auto kern = gemm_tc_kernel<BN, EPI, TF32>;
   static int configured_device = -1;  // attribute is per device; cheap to repeat
@@ -449,9 +498,14 @@ cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmW, int M, in
     configured_device = dev;
   }
   const int tiles = ((M + BM - 1) / BM) * (N / BN);
-  const int grid = tiles < num_sms ? tiles : num_sms;
-  return wenc_host::launch_pdl(kern, dim3(grid), dim3(kThreads), C::SMEM, stream, tmA, tmW, M, N, K, bias, resid, out,
-                               err, row_period, ex);
+  int grid = tiles < num_sms ? tiles : num_sms;
+  // The last partial wave, when it would leave at least half of the SMs idle, runs as twice as
+  // many half-width units (all tiles, when there are fewer than half as many as SMs).
+  const int n_tail = tiles < num_sms ? tiles : tiles % num_sms;
+  const int halves = (n_tail > 0 && 2 * n_tail <= num_sms) ? 1 : 0;
+  if (halves && tiles < num_sms) grid = 2 * tiles;
+  return wenc_host::launch_pdl(kern, dim3(grid), dim3(kThreads), C::SMEM, stream, tmA, tmW, tmW_half ? *tmW_half : tmW,
+                               tmW_half ? 1 : 0, M, N, K, bias, resid, out, err, row_period, ex, halves);
 }
 
 }  // namespace
@@ -466,7 +520,8 @@ int gemm_pick_bn(int N) {
 
 cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmW, int M, int N, int K, int bn, int epilogue,
                         const float* bias, const float* resid, void* out, uint32_t* err, int num_sms,
-                        cudaStream_t stream, bool tf32, int row_period, const GemmExtra& ex) {
+                        cudaStream_t stream, bool tf32, int row_period, const GemmExtra& ex,
+                        const CUtensorMap* tmW_half) {
   if (M <= 0) return cudaSuccess;
   if (epilogue == 5 &&
       (!ex.colsum || !ex.stats || ex.seg_w <= 0 || K % ex.seg_w != 0 || K / ex.seg_w > 32 || tf32))
@@ -476,7 +531,7 @@ cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmW, int M, i
   if (epilogue == 4 && (row_period <= 0 || row_period % 32 != 0 || N % row_period != 0)) return cudaErrorInvalidValue;
 #define WENC_GEMM_CASE(BNV, EPIV, TF) \
   if (bn == BNV && epilogue == EPIV && tf32 == TF)                                        \
-    return launch_one<BNV, EPIV, TF>(tmA, tmW, M, N, K, bias, resid, out, err, num_sms, stream, row_period, ex);
+    return launch_one<BNV, EPIV, TF>(tmA, tmW, tmW_half, M, N, K, bias, resid, out, err, num_sms, stream, row_period, ex);
   WENC_GEMM_CASE(256, 0, false)
   WENC_GEMM_CASE(256, 1, false)
   WENC_GEMM_CASE(256, 2, false)

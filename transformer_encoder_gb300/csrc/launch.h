@@ -93,9 +93,12 @@ constexpr int kEpiResidStats = 7;
 // Epilogue 4 (internal, the cross K/V precompute): as epilogue 0, written as planes of width
 // row_period: out[(col / P) * M * P + row * P + col % P]. P % 32 == 0 and N % P == 0.
 constexpr int kEpiBiasPlanes = 4;
+// tmW_half (optional): the same W with a box of bn / 2 rows, which the half-width units of a
+// split last wave load instead of full-height tiles.
 cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmW, int M, int N, int K, int bn, int epilogue,
                         const float* bias, const float* resid, void* out, uint32_t* err, int num_sms,
-                        cudaStream_t stream, bool tf32 = false, int row_period = 0, const GemmExtra& ex = GemmExtra());
+                        cudaStream_t stream, bool tf32 = false, int row_period = 0, const GemmExtra& ex = GemmExtra(),
+                        const CUtensorMap* tmW_half = nullptr);
 
 // ---------------------------------------------------------------- attention (tcgen05)
 // Q/K/V tiles are read through 3-D maps [B][T][row] (box 64 x 128 elements for all three);
