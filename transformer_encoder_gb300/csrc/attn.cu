@@ -25,6 +25,9 @@
 //    than 2^8. The two tiles take turns on the exponentials (ping-pong), so one tile's exps run
 //    while the other tile loads scores, stores P or waits, and the tensor pipe runs the other
 //    tile's products meanwhile. No T x T score buffer exists.
+// The control warpgroup (warps 0-3) hands registers to the softmax warpgroups at start-up
+// (setmaxnreg: 104 and 200 per thread instead of 168 for all), which keeps a row's scores and the
+// exponential pipeline in registers (211 -> 197 us at large-v3 dims, B = 16).
 // Key tiles of 128 make the S products full-rate (N = 128); the PV products have N = hd = 64.
 #include <cuda_bf16.h>
 #include <math_constants.h>
@@ -54,6 +57,14 @@ constexpr int HD = 64;
 constexpr int NK = 3;                     // K ring depth
 constexpr int NV = 3;                     // V ring depth
 constexpr int kThreads = 384;             // producer, 3 MMA issuers, 2 softmax warpgroups
+// Registers per thread after the start-up reallocation (setmaxnreg): the control warpgroup
+// (producer and MMA issuers) gives up registers that the two softmax warpgroups take, which keeps
+// a row's 128 scores and the exponential pipeline out of local memory. The sum must fit in what
+// the CTA is launched with (checked on the host before the first launch).
+constexpr int kCtrlRegs = 104;
+constexpr int kSoftmaxRegs = 200;
+constexpr int kRegsNeeded = kCtrlRegs * 128 + kSoftmaxRegs * 256;
+static_assert(kRegsNeeded <= (65536 / kThreads) / 8 * 8 * kThreads, "register split exceeds the launch budget");
 
 constexpr uint32_t Q_BYTES = BQ * HD * 2;           // 16 KB per query tile
 constexpr uint32_t KV_BYTES = BKV * HD * 2;         // 16 KB per K or V tile
@@ -165,105 +176,110 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // Every role walks the same items in the same order and counts K/V tiles across them (kc,
   // vc, g below), so ring slots and barrier parities continue from one item to the next.
-  if (warp == 0 && lane == 0) {
-    // ---------------- TMA producer, per item: Q_A, Q_B into the item's Q buffer (free once the
-    // S products of the item two back are done), then K0, then (K[j], V[j-1]) for j >= 1, then
-    // V[n-1]; the next item's Q and first K tiles load while this item's last tiles run.
-    int kc = 0, vc = 0, qi = 0;  // K tiles, V tiles and items issued
-    auto load_k = [&](const Item& it, int j) -> bool {
-      const int st = kc % NK;
-      if (!mbar_wait(k_empty(st), ((kc / NK) & 1) ^ 1u, wc, 11)) return false;
-      mbar_arrive_expect_tx(k_full(st), KV_BYTES);
-      tma_load_3d(sK + st * KV_BYTES, &tk, k_full(st), k_col0 + it.h * HD, (it.kv0 + j) * BKV, it.b);
-      ++kc;
-      return true;
-    };
-    auto load_v = [&](const Item& it, int j) -> bool {
-      const int st = vc % NV;
-      if (!mbar_wait(v_empty(st), ((vc / NV) & 1) ^ 1u, wc, 10)) return false;
-      mbar_arrive_expect_tx(v_full(st), KV_BYTES);
-      tma_load_3d(sV + st * KV_BYTES, &tv, v_full(st), v_col0 + it.h * HD, (it.kv0 + j) * BKV, it.b);
-      ++vc;
-      return true;
-    };
-    bool ok = true;
-    for (int w = blockIdx.x, i = 0; ok && w < n_items; w += gridDim.x, ++i) {
-      const Item it = decode(w);
-      const int qb = i & 1;
-      if (!mbar_wait(q_empty(qb), ((i >> 1) & 1) ^ 1u, wc, 9)) break;
-      mbar_arrive_expect_tx(q_full(qb), 2 * Q_BYTES);
-      tma_load_3d(sQ + qb * 2 * Q_BYTES, &tq, q_full(qb), q_col0 + it.h * HD, it.q0, it.b);
-      tma_load_3d(sQ + qb * 2 * Q_BYTES + Q_BYTES, &tq, q_full(qb), q_col0 + it.h * HD, it.q0 + BQ, it.b);
-      qi = i + 1;
-      for (int j = 0; ok && j <= it.n_kv; ++j) {
-        if (j < it.n_kv) ok = load_k(it, j);
-        if (ok && j >= 1) ok = load_v(it, j - 1);
-      }
-    }
-    if (*abort_flag) {
-      // Error path: let the copies already issued land before the CTA exits.
-      for (int u = (qi > 2 ? qi - 2 : 0); u < qi; ++u) mbar_wait_drain(q_full(u & 1), (u >> 1) & 1);
-      for (int j = (kc > NK ? kc - NK : 0); j < kc; ++j) mbar_wait_drain(k_full(j % NK), (j / NK) & 1);
-      for (int j = (vc > NV ? vc - NV : 0); j < vc; ++j) mbar_wait_drain(v_full(j % NV), (j / NV) & 1);
-    }
-  } else if (warp >= 1 && warp <= 3 && lane == 0) {
-    // ---------------- UMMA issuers. A single thread cannot issue MMAs fast enough to keep the
-    // tensor pipe busy with N = 64 products, so three threads share the work: warp 1 issues
-    // S_A = Q_A K_j^T and S_B = Q_B K_j^T as soon as the scores of tile j-1 have been read;
-    // warps 2 and 3 issue O_A += P_A V_j and O_B += P_B V_j once P of tile j is written.
-    // Descriptors are built once per operand tile; a K step of 16 elements advances the start
-    // address by 32 bytes (K-major, inside the 128-byte swizzle row: +2 in the >>4 field) or by
-    // 16 rows of 128 bytes (the MN-major V tile: +128).
-    bool ok = true;
-    if (warp == 1) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(BQ, BKV, false);  // B = K tile, K-major, N = 128
-      int kc = 0;  // K tiles consumed, across items
+  if (warp < 4) {
+    // control warpgroup: registers to the softmax warpgroups first
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kCtrlRegs) : "memory");
+    if (warp == 0 && lane == 0) {
+      // ---------------- TMA producer, per item: Q_A, Q_B into the item's Q buffer (free once the
+      // S products of the item two back are done), then K0, then (K[j], V[j-1]) for j >= 1, then
+      // V[n-1]; the next item's Q and first K tiles load while this item's last tiles run.
+      int kc = 0, vc = 0, qi = 0;  // K tiles, V tiles and items issued
+      auto load_k = [&](const Item& it, int j) -> bool {
+        const int st = kc % NK;
+        if (!mbar_wait(k_empty(st), ((kc / NK) & 1) ^ 1u, wc, 11)) return false;
+        mbar_arrive_expect_tx(k_full(st), KV_BYTES);
+        tma_load_3d(sK + st * KV_BYTES, &tk, k_full(st), k_col0 + it.h * HD, (it.kv0 + j) * BKV, it.b);
+        ++kc;
+        return true;
+      };
+      auto load_v = [&](const Item& it, int j) -> bool {
+        const int st = vc % NV;
+        if (!mbar_wait(v_empty(st), ((vc / NV) & 1) ^ 1u, wc, 10)) return false;
+        mbar_arrive_expect_tx(v_full(st), KV_BYTES);
+        tma_load_3d(sV + st * KV_BYTES, &tv, v_full(st), v_col0 + it.h * HD, (it.kv0 + j) * BKV, it.b);
+        ++vc;
+        return true;
+      };
+      bool ok = true;
       for (int w = blockIdx.x, i = 0; ok && w < n_items; w += gridDim.x, ++i) {
-        const int n_kv = decode(w).n_kv;
+        const Item it = decode(w);
         const int qb = i & 1;
-        if (!mbar_wait(q_full(qb), (i >> 1) & 1, wc, 12)) break;
-        for (int j = 0; ok && j < n_kv; ++j, ++kc) {
-          const int st = kc % NK;
-          if (!mbar_wait(k_full(st), (kc / NK) & 1, wc, 13)) { ok = false; break; }
-          const uint64_t kdesc = sdesc_sw128(sK + st * KV_BYTES, 16, 1024);
-          for (int t = 0; t < 2 && ok; ++t) {
-            if (kc >= 1 && !mbar_wait(s_free(t), (kc - 1) & 1, wc, 14)) { ok = false; break; }
+        if (!mbar_wait(q_empty(qb), ((i >> 1) & 1) ^ 1u, wc, 9)) break;
+        mbar_arrive_expect_tx(q_full(qb), 2 * Q_BYTES);
+        tma_load_3d(sQ + qb * 2 * Q_BYTES, &tq, q_full(qb), q_col0 + it.h * HD, it.q0, it.b);
+        tma_load_3d(sQ + qb * 2 * Q_BYTES + Q_BYTES, &tq, q_full(qb), q_col0 + it.h * HD, it.q0 + BQ, it.b);
+        qi = i + 1;
+        for (int j = 0; ok && j <= it.n_kv; ++j) {
+          if (j < it.n_kv) ok = load_k(it, j);
+          if (ok && j >= 1) ok = load_v(it, j - 1);
+        }
+      }
+      if (*abort_flag) {
+        // Error path: let the copies already issued land before the CTA exits.
+        for (int u = (qi > 2 ? qi - 2 : 0); u < qi; ++u) mbar_wait_drain(q_full(u & 1), (u >> 1) & 1);
+        for (int j = (kc > NK ? kc - NK : 0); j < kc; ++j) mbar_wait_drain(k_full(j % NK), (j / NK) & 1);
+        for (int j = (vc > NV ? vc - NV : 0); j < vc; ++j) mbar_wait_drain(v_full(j % NV), (j / NV) & 1);
+      }
+    } else if (warp >= 1 && warp <= 3 && lane == 0) {
+      // ---------------- UMMA issuers. A single thread cannot issue MMAs fast enough to keep the
+      // tensor pipe busy with N = 64 products, so three threads share the work: warp 1 issues
+      // S_A = Q_A K_j^T and S_B = Q_B K_j^T as soon as the scores of tile j-1 have been read;
+      // warps 2 and 3 issue O_A += P_A V_j and O_B += P_B V_j once P of tile j is written.
+      // Descriptors are built once per operand tile; a K step of 16 elements advances the start
+      // address by 32 bytes (K-major, inside the 128-byte swizzle row: +2 in the >>4 field) or by
+      // 16 rows of 128 bytes (the MN-major V tile: +128).
+      bool ok = true;
+      if (warp == 1) {
+        constexpr uint32_t idesc_s = idesc_bf16_f32(BQ, BKV, false);  // B = K tile, K-major, N = 128
+        int kc = 0;  // K tiles consumed, across items
+        for (int w = blockIdx.x, i = 0; ok && w < n_items; w += gridDim.x, ++i) {
+          const int n_kv = decode(w).n_kv;
+          const int qb = i & 1;
+          if (!mbar_wait(q_full(qb), (i >> 1) & 1, wc, 12)) break;
+          for (int j = 0; ok && j < n_kv; ++j, ++kc) {
+            const int st = kc % NK;
+            if (!mbar_wait(k_full(st), (kc / NK) & 1, wc, 13)) { ok = false; break; }
+            const uint64_t kdesc = sdesc_sw128(sK + st * KV_BYTES, 16, 1024);
+            for (int t = 0; t < 2 && ok; ++t) {
+              if (kc >= 1 && !mbar_wait(s_free(t), (kc - 1) & 1, wc, 14)) { ok = false; break; }
+              tc_fence_after();
+              const uint64_t qdesc = sdesc_sw128(sQ + qb * 2 * Q_BYTES + t * Q_BYTES, 16, 1024);
+#pragma unroll
+              for (int k = 0; k < HD / 16; ++k) umma_bf16_ss(tS(t), qdesc + k * 2, kdesc + k * 2, idesc_s, k > 0);
+              umma_commit(s_full(t));
+            }
+            if (ok) umma_commit(k_empty(st));
+          }
+          if (ok) umma_commit(q_empty(qb));  // the item's Q buffer is free once its S products are done
+        }
+      } else {
+        constexpr uint32_t idesc_o = idesc_bf16_f32(BQ, HD, true);  // B = V tile, MN-major, N = 64
+        const int t = warp - 2;
+        int vc = 0;  // V tiles consumed, across items
+        for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+          const int n_kv = decode(w).n_kv;
+          for (int j = 0; j < n_kv; ++j, ++vc) {
+            const int st = vc % NV;
+            if (!mbar_wait(v_full(st), (vc / NV) & 1, wc, 15) || !mbar_wait(p_full(t), vc & 1, wc, 16)) {
+              ok = false;
+              break;
+            }
             tc_fence_after();
-            const uint64_t qdesc = sdesc_sw128(sQ + qb * 2 * Q_BYTES + t * Q_BYTES, 16, 1024);
+            const uint64_t vdesc = sdesc_sw128(sV + st * KV_BYTES, 1024, 1024);
 #pragma unroll
-            for (int k = 0; k < HD / 16; ++k) umma_bf16_ss(tS(t), qdesc + k * 2, kdesc + k * 2, idesc_s, k > 0);
-            umma_commit(s_full(t));
+            for (int k = 0; k < BKV / 16; ++k)
+              umma_bf16_ts(tO(t), tP(t) + 8 * k, vdesc + k * 128, idesc_o, (j > 0 || k > 0) ? 1u : 0u);
+            umma_commit(pv_done(t));
+            umma_commit(v_empty(st));
           }
-          if (ok) umma_commit(k_empty(st));
-        }
-        if (ok) umma_commit(q_empty(qb));  // the item's Q buffer is free once its S products are done
-      }
-    } else {
-      constexpr uint32_t idesc_o = idesc_bf16_f32(BQ, HD, true);  // B = V tile, MN-major, N = 64
-      const int t = warp - 2;
-      int vc = 0;  // V tiles consumed, across items
-      for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
-        const int n_kv = decode(w).n_kv;
-        for (int j = 0; j < n_kv; ++j, ++vc) {
-          const int st = vc % NV;
-          if (!mbar_wait(v_full(st), (vc / NV) & 1, wc, 15) || !mbar_wait(p_full(t), vc & 1, wc, 16)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t vdesc = sdesc_sw128(sV + st * KV_BYTES, 1024, 1024);
-#pragma unroll
-          for (int k = 0; k < BKV / 16; ++k)
-            umma_bf16_ts(tO(t), tP(t) + 8 * k, vdesc + k * 128, idesc_o, (j > 0 || k > 0) ? 1u : 0u);
-          umma_commit(pv_done(t));
-          umma_commit(v_empty(st));
         }
       }
+      // Every MMA this thread issued completes before TMEM is released.
+      umma_commit(drain);
+      mbar_wait_drain(drain, 0);
     }
-    // Every MMA this thread issued completes before TMEM is released.
-    umma_commit(drain);
-    mbar_wait_drain(drain, 0);
-  } else if (warp >= 4) {
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kSoftmaxRegs) : "memory");
     // ---------------- softmax / correction / output: one query row per thread
     const int t = (warp - 4) >> 2;  // query tile of this warpgroup
     const int quad = warp & 3;
@@ -509,6 +525,11 @@ cudaError_t launch_attention_main(const CUtensorMap& tq, const CUtensorMap& tk, 
   if (configured_device != dev) {
     cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM));
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+    // The softmax warpgroups' register increase is met only from the registers the CTA was
+    // launched with: refuse to launch a build that was given fewer.
+    cudaFuncAttributes fa;
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, attn_fwd_kernel);
+    if (e == cudaSuccess && fa.numRegs * kThreads < kRegsNeeded) e = cudaErrorInvalidConfiguration;
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
