@@ -102,8 +102,8 @@ cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmW, int M, i
 
 // ---------------------------------------------------------------- attention (tcgen05)
 // Q/K/V tiles are read through 3-D maps [B][T][row] (box 64 x 128 elements for all three);
-// head h of Q, K, V starts at column q_col0 + 64h, k_col0 + 64h, v_col0 + 64h. One CTA covers
-// 2 * kAttnBQ query rows of one (window, head).
+// head h of Q, K, V starts at column q_col0 + 64h, k_col0 + 64h, v_col0 + 64h. A persistent grid
+// (one CTA per SM) walks work items of 2 * kAttnBQ query rows of one (window, head).
 // out: bf16, row (b*T + t) at out + (b*T+t)*out_stride + 64h.
 // With n_splits > 1 the key tiles are divided among n_splits CTAs per query pair, which write
 // unnormalised partial results to part_o [n_splits*B*H*T, 64] and (max, sum) to part_ml; a second
@@ -127,7 +127,8 @@ int attention_launches(int T, int n_splits);  // kernels one launch_attention ma
 
 // TF32 attention: Q/K/V fp32 [B][T][row] through 3-D fp32 maps (box 32 x 128 for Q, 32 x
 // kAttnTf32BKV for K and V; each 64-wide head is read as two 32-column boxes); out fp32
-// rounded to TF32, row (b*T+t) at out + (b*T+t)*out_stride + 64h. One CTA per 2 x 128 queries.
+// rounded to TF32, row (b*T+t) at out + (b*T+t)*out_stride + 64h. A persistent grid walks work
+// items of 2 x 128 queries of one (window, head).
 constexpr int kAttnTf32BQ = 128;
 constexpr int kAttnTf32BKV = 64;
 cudaError_t launch_attention_tf32(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, int q_col0,
