@@ -295,13 +295,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait_warp(s_full(t), g & 1, wc, 17)) { ok = false; break; }
         tc_fence_after();
         float sv[128];
+        {
+          // the row's 128 scores: four loads in flight, one wait
+          uint32_t r[4][32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(tS(t) + lane_off + c * 32, r);
+          for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(tS(t) + lane_off + c * 32, r[c]);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) sv[c * 32 + e] = __uint_as_float(r[e]);
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) sv[c * 32 + e] = __uint_as_float(r[c][e]);
         }
         tc_fence_before();
         __syncwarp();
