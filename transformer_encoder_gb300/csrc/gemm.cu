@@ -18,7 +18,7 @@
 // Design (sm_103a): persistent CTAs, one per SM, walk 128 x BN output tiles. Warp 0 is the
 // TMA producer (A and W tiles, 128-byte swizzle, a STAGES-deep mbarrier ring); warp 1
 // allocates TMEM and one of its threads issues tcgen05.mma (128 x BN x 16, bf16 in, fp32
-// accumulate) into one of two TMEM accumulators; warps 2-5 drain the other accumulator
+// accumulate) into one of two TMEM accumulators; warps 2-9 drain the other accumulator
 // (tcgen05.ld -> bias / GELU / residual -> global) while the next tile is being computed.
 #include <cuda_bf16.h>
 
