@@ -167,6 +167,34 @@ def test_windows_independent_of_batch_large_dims(precision):
     assert torch.equal(last[0], full[-1])
 
 
+@pytest.mark.parametrize("wname,precision", [("tiny_stack", "bf16"), ("large_pair", "bf16"), ("large_pair", "tf32")])
+def test_forward_captures_in_a_cuda_graph(wname, precision):
+    """wenc_forward is stream-ordered and allocates nothing, so it can be captured into a CUDA
+    graph (its launches keep their programmatic dependencies as graph edges); a replay gives the
+    same bits as the eager call."""
+    import torch
+    w = synth.WORKLOADS[wname]
+    enc, _, _, rng = make_encoder(w, keep_host_layers=False, precision=precision)
+    x = _t(synth.make_input(w, rng))
+    ref = enc.forward(x)
+    out = torch.empty_like(x)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        enc.forward(x, out)  # a call on the capture stream before capturing
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        enc.forward(x, out)
+    out.zero_()
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    enc.sync_status()
+    assert torch.equal(out, ref)
+
+
 def test_argument_errors():
     import torch
     from transformer_encoder_gb300 import WencError
