@@ -33,6 +33,8 @@
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
+#include <atomic>
+
 #include "launch.h"
 #include "ptx.cuh"
 
@@ -522,21 +524,26 @@ cudaError_t launch_attention_main(const CUtensorMap& tq, const CUtensorMap& tk, 
                                   int k_col0, int v_col0, uint16_t* out, int out_stride, int B, int T, int H,
                                   uint32_t* err, cudaStream_t stream, int n_splits, float* part_o, float2* part_ml) {
   if (B <= 0 || T <= 0 || H <= 0) return cudaSuccess;
-  static int configured_device = -1;
-  static int num_sms = 0;
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM));
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
-    // The softmax warpgroups' register increase is met only from the registers the CTA was
-    // launched with: refuse to launch a build that was given fewer.
-    cudaFuncAttributes fa;
-    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, attn_fwd_kernel);
-    if (e == cudaSuccess && fa.numRegs * kThreads < kRegsNeeded) e = cudaErrorInvalidConfiguration;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  // Shared-memory opt-in, once per device (a repeat by a racing host thread is harmless).
+  static std::atomic<int> configured_device{-1};
+  if (configured_device.load(std::memory_order_acquire) != dev) {
+    e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM));
     if (e != cudaSuccess) return e;
-    configured_device = dev;
+    configured_device.store(dev, std::memory_order_release);
   }
+  // The softmax warpgroups' register increase is met only from the registers the CTA was
+  // launched with: refuse to launch a build that was given fewer (a property of the build).
+  static const int launch_regs = [] {
+    cudaFuncAttributes fa;
+    return cudaFuncGetAttributes(&fa, attn_fwd_kernel) == cudaSuccess ? fa.numRegs : 0;
+  }();
+  if (launch_regs * kThreads < kRegsNeeded) return cudaErrorInvalidConfiguration;
+  int num_sms = 0;
+  e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
   const float scale_log2 = 1.4426950408889634f / 8.0f;  // log2(e) / sqrt(64)
   if (!part_o || !part_ml) n_splits = 1;
   n_splits = clamp_splits(T, n_splits);

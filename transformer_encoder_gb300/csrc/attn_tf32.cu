@@ -32,6 +32,8 @@
 // transpose in the producer warp to free a warp for a third issuer was slower.)
 #include <math_constants.h>
 
+#include <atomic>
+
 #include "launch.h"
 #include "ptx.cuh"
 
@@ -442,16 +444,19 @@ cudaError_t launch_attention_tf32(const CUtensorMap& tq, const CUtensorMap& tk, 
                                   int k_col0, int v_col0, float* out, int out_stride, int B, int T, int H,
                                   uint32_t* err, cudaStream_t stream) {
   if (B <= 0 || T <= 0 || H <= 0) return cudaSuccess;
-  static int configured_device = -1;
-  static int num_sms = 0;
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tf32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM));
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  // Shared-memory opt-in, once per device (a repeat by a racing host thread is harmless).
+  static std::atomic<int> configured_device{-1};
+  if (configured_device.load(std::memory_order_acquire) != dev) {
+    e = cudaFuncSetAttribute(attn_tf32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM));
     if (e != cudaSuccess) return e;
-    configured_device = dev;
+    configured_device.store(dev, std::memory_order_release);
   }
+  int num_sms = 0;
+  e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
   const float scale_log2 = 1.4426950408889634f / 8.0f;  // log2(e) / sqrt(64)
   const long long items = static_cast<long long>((T + 2 * BQ - 1) / (2 * BQ)) * H * B;
   if (items > (1LL << 30)) return cudaErrorInvalidValue;

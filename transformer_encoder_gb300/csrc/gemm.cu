@@ -22,6 +22,8 @@
 // (tcgen05.ld -> bias / GELU / residual -> global) while the next tile is being computed.
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include "launch.h"
 #include "ptx.cuh"
 
@@ -489,13 +491,16 @@ cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmW, const CUt
                        cudaStream_t stream, int row_period, const wenc_host::GemmExtra& ex) {
   using C = GemmCfg<BN>;
   auto kern = gemm_tc_kernel<BN, EPI, TF32>;
-  static int configured_device = -1;  // attribute is per device; cheap to repeat
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM));
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  // Shared-memory opt-in, once per device and instantiation (a repeat by a racing host thread
+  // is harmless).
+  static std::atomic<int> configured_device{-1};
+  if (configured_device.load(std::memory_order_acquire) != dev) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM));
     if (e != cudaSuccess) return e;
-    configured_device = dev;
+    configured_device.store(dev, std::memory_order_release);
   }
   const int tiles = ((M + BM - 1) / BM) * (N / BN);
   int grid = tiles < num_sms ? tiles : num_sms;
