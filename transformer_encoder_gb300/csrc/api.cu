@@ -11,6 +11,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -74,22 +75,25 @@ EncodeTiledFn encode_fn() {
 __device__ uint32_t g_device_error_word;
 
 uint32_t* global_error_word(std::string* why) {
-  static uint32_t* addr[64] = {nullptr};
+  // per-device cache; host threads that race here store the same address
+  static std::atomic<uint32_t*> addr[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
     *why = "no current CUDA device";
     return nullptr;
   }
-  if (!addr[dev]) {
+  uint32_t* a = addr[dev].load(std::memory_order_acquire);
+  if (!a) {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_device_error_word);
     if (e != cudaSuccess) {
       *why = std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e);
       return nullptr;
     }
-    addr[dev] = static_cast<uint32_t*>(p);
+    a = static_cast<uint32_t*>(p);
+    addr[dev].store(a, std::memory_order_release);
   }
-  return addr[dev];
+  return a;
 }
 
 bool device_is_sm103(std::string* why) {
