@@ -195,6 +195,48 @@ def test_forward_captures_in_a_cuda_graph(wname, precision):
     assert torch.equal(out, ref)
 
 
+def test_concurrent_handles_from_two_host_threads():
+    """Two host threads drive their own handles on their own streams at the same time (the
+    binding releases the interpreter lock during library calls); every result equals the
+    single-threaded one bit for bit, and the first calls of both threads race through the
+    launchers' one-time set-up."""
+    import threading
+    import torch
+    w = synth.WORKLOADS["tiny_stack"]
+    encs, xs, refs = [], [], []
+    for seed in (11, 12):
+        enc, _, _, rng = make_encoder(w, keep_host_layers=False)
+        x = _t(synth.make_input(w, np.random.default_rng(seed)))
+        encs.append(enc)
+        xs.append(x)
+    outs = [[None] * 6 for _ in range(2)]
+    errors = []
+
+    def run(i):
+        try:
+            stream = torch.cuda.Stream()
+            with torch.cuda.stream(stream):
+                for k in range(6):
+                    outs[i][k] = encs[i].forward(xs[i])
+            stream.synchronize()
+        except Exception as e:  # surfaced below
+            errors.append(e)
+
+    threads = [threading.Thread(target=run, args=(i,)) for i in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    torch.cuda.synchronize()
+    for i in range(2):
+        encs[i].sync_status()
+        ref = encs[i].forward(xs[i])
+        torch.cuda.synchronize()
+        for k in range(6):
+            assert torch.equal(outs[i][k], ref)
+
+
 def test_argument_errors():
     import torch
     from transformer_encoder_gb300 import WencError
