@@ -20,7 +20,11 @@
  *  - Weight matrices are [n_out, n_in] row-major (PyTorch layout); y = x W^T + b.
  *  - bf16 buffers are raw bfloat16 bit patterns (uint16_t).
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream).
- *    Entry points marked "stream-ordered" do not synchronise the host and allocate nothing.
+ *    Entry points marked "stream-ordered" do not synchronise the host and allocate nothing,
+ *    so a call can be captured into a CUDA graph (make one ordinary call first: the first
+ *    call on a device does one-time set-up); a replay gives the bits of an eager call.
+ *  - Separate handles may be used from separate host threads at the same time. Calls on one
+ *    handle share its workspace and must be ordered by the caller (one stream, or events).
  *  - Argument errors are reported synchronously as a status; the message is available
  *    from wenc_last_error() on the same host thread. Nothing aborts the process.
  *  - Device-side waits are bounded (about one second); a wait that runs out records
