@@ -931,12 +931,14 @@ wenc_status wenc_linear(const uint16_t* A, const uint16_t* W, const float* bias,
   if (!device_is_sm103(&why)) return fail(WENC_ERR_UNSUPPORTED, "%s", why.c_str());
   uint32_t* err = global_error_word(&why);
   if (!err) return fail(WENC_ERR_CUDA, "%s", why.c_str());
-  CUtensorMap ta, tw;
+  CUtensorMap ta, tw, tw_h;
   bool ok = wenc_host::make_tmap_2d_bf16(&ta, A, K, M, size_t(K) * 2, 64, wenc_host::kGemmBM, &why) &&
-            wenc_host::make_tmap_2d_bf16(&tw, W, K, N, size_t(K) * 2, 64, bn, &why);
+            wenc_host::make_tmap_2d_bf16(&tw, W, K, N, size_t(K) * 2, 64, bn, &why) &&
+            wenc_host::make_tmap_2d_bf16(&tw_h, W, K, N, size_t(K) * 2, 64, bn / 2, &why);
   if (!ok) return fail(WENC_ERR_INVALID_ARG, "%s", why.c_str());
   cudaError_t e = wenc_host::launch_gemm(ta, tw, M, N, K, bn, epilogue, bias, resid, out, err, sm_count(),
-                                         reinterpret_cast<cudaStream_t>(stream));
+                                         reinterpret_cast<cudaStream_t>(stream), false, 0, wenc_host::GemmExtra(),
+                                         &tw_h);
   if (e != cudaSuccess) return cuda_fail(e, "linear launch");
   return WENC_OK;
 }

@@ -21,6 +21,7 @@
 // accumulate) into one of two TMEM accumulators; warps 2-9 drain the other accumulator
 // (tcgen05.ld -> bias / GELU / residual -> global) while the next tile is being computed.
 #include <cuda_bf16.h>
+#include <stdlib.h>
 
 #include <atomic>
 
@@ -36,12 +37,16 @@ constexpr int BK = wenc_host::kGemmBK;
 constexpr int kEpiWarps = 8;                // two warps per TMEM lane quadrant
 constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer warp, MMA warp, epilogue warps
 
-template <int BN>
+// PAIR: a CTA pair (a cluster of two on one TPC) computes a 256 x BN tile with M256 MMAs
+// (tcgen05 cta_group::2): each CTA holds its 128 rows of A and BN / 2 rows of W per stage, the
+// pair's even CTA issues the MMAs, and each CTA's TMEM receives its own 128 rows. Half of W per
+// CTA leaves room for six stages instead of four in the same shared memory.
+template <int BN, bool PAIR = false>
 struct GemmCfg {
-  static constexpr int STAGES = (BN == 256) ? 4 : 6;
+  static constexpr int STAGES = PAIR ? 6 : (BN == 256) ? 4 : 6;
   // One stage holds 128-byte rows: 64 bf16 or 32 fp32 elements of K.
   static constexpr uint32_t A_BYTES = BM * 128;
-  static constexpr uint32_t B_BYTES = BN * 128;
+  static constexpr uint32_t B_BYTES = (PAIR ? BN / 2 : BN) * 128;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TMEM_COLS = 2 * BN;  // two fp32 accumulators of BN columns
   static constexpr uint32_t NUM_BARS = 2 * STAGES + 5;
@@ -76,6 +81,90 @@ __device__ __forceinline__ void gelu_erf_x2(float& z0, float& z1) {
   unpack_f32x2(fma_f32x2(poly, neg_e, pack_f32x2(1.0f, 1.0f)), r0, r1);  // erf(|x|)
   const uint64_t one_p = pack_f32x2(1.0f + copysignf(r0, z0), 1.0f + copysignf(r1, z1));  // 1 + erf(x)
   unpack_f32x2(mul_f32x2(mul_f32x2(pack_f32x2(z0, z1), pack_f32x2(0.5f, 0.5f)), one_p), z0, z1);
+}
+
+// ---- CTA-pair forms (cluster of two CTAs; every tcgen05 instruction of a pair kernel uses
+// cta_group::2, as the PTX ISA requires one cta_group value per kernel)
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of both CTAs; release / acquire at cluster scope.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The shared::cluster address of the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// Bounded wait (as mbar_wait) that acquires at cluster scope: for barriers the peer CTA arrives on.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, const WaitCtx& w, uint32_t site) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((n & 3u) == 0) {
+      if (*w.abort_flag) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        *w.abort_flag = 1u;
+        *reinterpret_cast<volatile uint32_t*>(w.err) = kErrTimeout | (site << 8);
+        return false;
+      }
+    }
+  }
+}
+// TMA tile load into this CTA's shared memory whose completion is counted on `bar_cluster`,
+// a barrier of either CTA of the pair (shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster, int x,
+                                                 int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], "
+      "[%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// D (both CTAs' TMEM at d_tmem) (+)= A (each CTA's 128 rows) * B^T (BN / 2 rows from each CTA).
+__device__ __forceinline__ void umma_bf16_ss_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                  uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on the barrier at offset `bar` of every CTA in `cta_mask` when the MMAs issued so
+// far have completed.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar, uint16_t cta_mask) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   bar),
+               "h"(cta_mask)
+               : "memory");
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -187,13 +276,14 @@ __device__ __forceinline__ void epilogue_chunk(const uint32_t (&acc)[32], uint32
   __syncwarp();  // the stage is rewritten by the next chunk
 }
 
-template <int BN, int EPI, bool TF32>
+template <int BN, int EPI, bool TF32, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                    const __grid_constant__ CUtensorMap tmWh, int half_box, int M, int N,
                    int K, const float* __restrict__ bias, const float* resid, void* out, uint32_t* err,
                    int row_period, const wenc_host::GemmExtra ex, int tail_halves) {
-  using C = GemmCfg<BN>;
+  static_assert(!PAIR || (!TF32 && BN == 256), "CTA pairs run the bf16 256-column tiles");
+  using C = GemmCfg<BN, PAIR>;
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -212,7 +302,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int m_tiles = (M + BM - 1) / BM;
+  // The scheduling unit: a CTA, or a CTA pair (rank 0 or 1 within it) working on 256-row tiles.
+  constexpr int TM = PAIR ? 2 * BM : BM;  // output rows per tile
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int n_units = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  const int m_tiles = (M + TM - 1) / TM;
   const int n_tiles = N / BN;
   const int num_tiles = m_tiles * n_tiles;
   // Tile order. The block GEMMs walk n fastest: a wave of CTAs shares one A row block, and W
@@ -237,28 +332,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   constexpr int BKE = TF32 ? 32 : BK;  // K elements per stage (128-byte rows)
   const int k_blocks = K / BKE;
-  // Work items of this CTA, the same sequence for every role: whole tiles blockIdx.x + i G
-  // (G = gridDim.x) over the first n_dp tiles; then, when the launch splits its last partial
-  // wave (tail_halves), one half-width unit: the n_tail = num_tiles % G remaining tiles become
-  // 2 n_tail units of BN / 2 columns (an M128 N(BN/2) product over the whole K), unit
-  // u = blockIdx.x < 2 n_tail taking half u % 2 of tile n_dp + u / 2. Each output element is
-  // the same fixed-order dot product either way.
-  const int n_tail = tail_halves ? num_tiles % static_cast<int>(gridDim.x) : 0;
+  // Work items of this unit (CTA or pair), the same sequence for every role: whole tiles
+  // unit + i G (G = the number of units) over the first n_dp tiles; then, when the launch splits
+  // its last partial wave (tail_halves), one half-width unit: the n_tail = num_tiles % G
+  // remaining tiles become 2 n_tail units of BN / 2 columns (an M128 (pair: M256) N(BN/2)
+  // product over the whole K), unit u < 2 n_tail taking half u % 2 of tile n_dp + u / 2. Each
+  // output element is the same fixed-order dot product either way.
+  const int n_tail = tail_halves ? num_tiles % n_units : 0;
   const int n_dp = num_tiles - n_tail;
-  const int n_mine = (static_cast<int>(blockIdx.x) < n_dp)
-                         ? (n_dp - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
-                         : 0;
-  const bool has_unit = static_cast<int>(blockIdx.x) < 2 * n_tail;
-  // item i of this CTA: its tile and, for the half-width unit, which half (-1: the whole tile)
+  const int n_mine = (unit < n_dp) ? (n_dp - 1 - unit) / n_units + 1 : 0;
+  const bool has_unit = unit < 2 * n_tail;
+  // item i of this unit: its tile and, for the half-width unit, which half (-1: the whole tile)
   auto item = [&](int i, int& tile, int& half) -> bool {
     if (i < n_mine) {
-      tile = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
+      tile = unit + i * n_units;
       half = -1;
       return true;
     }
     if (i == n_mine && has_unit) {
-      tile = n_dp + static_cast<int>(blockIdx.x) / 2;
-      half = static_cast<int>(blockIdx.x) % 2;
+      tile = n_dp + unit / 2;
+      half = unit % 2;
       return true;
     }
     return false;
@@ -271,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), kEpiWarps);  // one arrival per epilogue warp
+      mbar_init(tempty_bar(a), PAIR ? 2 * kEpiWarps : kEpiWarps);  // one arrival per epilogue warp (of the pair)
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0u;
@@ -281,11 +374,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (half_box) tma_prefetch_desc(&tmWh);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_slot), C::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) {
+    __syncwarp();
+    cluster_sync_all();  // both CTAs' barriers are initialised before either signals the other's
+  } else {
+    __syncthreads();
+  }
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   pdl_trigger();  // TMEM is held: the next kernel may be scheduled
@@ -299,23 +402,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int tile, half;
     for (int i = 0; ok && item(i, tile, half); ++i) {
-      const int m0 = tile_m(tile) * BM;
+      // A pair's CTA loads its own 128 rows of A and its share of W (BN / 2 rows through the
+      // half-box map; BN / 4 of them in a half-width unit, the other rows of the box unused),
+      // counted on the even CTA's full barrier, which expects both CTAs' bytes.
+      const int m0 = tile_m(tile) * TM + static_cast<int>(rank) * BM;
       // a half-width unit loads BN / 2 rows of W through the half-box map (or, without one, the
       // BN rows from its half's first column, rows past N reading as zeros) and multiplies the
       // first BN / 2 of them
-      const int n0 = tile_n(tile) * BN + (half > 0 ? BN / 2 : 0);
+      const int n0 = tile_n(tile) * BN + (half > 0 ? BN / 2 : 0) +
+                     (PAIR ? static_cast<int>(rank) * (half < 0 ? BN / 2 : BN / 4) : 0);
       const bool hb = half >= 0 && half_box;
       const uint32_t stage_bytes = hb ? C::A_BYTES + C::B_BYTES / 2 : C::STAGE_BYTES;
       for (int kb = 0; kb < k_blocks; ++kb) {
         if (!mbar_wait(empty_bar(stage), phase ^ 1u, wc, 1)) { ok = false; break; }
-        mbar_arrive_expect_tx(full_bar(stage), stage_bytes);
-        tma_load_2d(sA + stage * C::A_BYTES, &tmA, full_bar(stage), kb * BKE, m0);
-        tma_load_2d(sB + stage * C::B_BYTES, hb ? &tmWh : &tmW, full_bar(stage), kb * BKE, n0);
+        if constexpr (PAIR) {
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * C::STAGE_BYTES);
+          const uint32_t lead_full = map_to_rank(full_bar(stage), 0);
+          tma_load_2d_pair(sA + stage * C::A_BYTES, &tmA, lead_full, kb * BKE, m0);
+          tma_load_2d_pair(sB + stage * C::B_BYTES, &tmWh, lead_full, kb * BKE, n0);
+        } else {
+          mbar_arrive_expect_tx(full_bar(stage), stage_bytes);
+          tma_load_2d(sA + stage * C::A_BYTES, &tmA, full_bar(stage), kb * BKE, m0);
+          tma_load_2d(sB + stage * C::B_BYTES, hb ? &tmWh : &tmW, full_bar(stage), kb * BKE, n0);
+        }
         issued_mask |= 1u << stage;
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
     }
-    if (!ok) {
+    if (!ok && PAIR && rank != 0) {
+      // Error path of the odd CTA: its copies count on the even CTA's barriers; give the ones
+      // in flight time to land (they take microseconds) before the CTA exits.
+      const uint64_t t0 = global_timer_ns();
+      while (global_timer_ns() - t0 < 200000ull) {
+      }
+    } else if (!ok) {
       // Error path: let the copies already issued land before the CTA exits.
       for (int s = 0; s < STAGES; ++s) {
         if (!(issued_mask & (1u << s))) continue;
@@ -323,11 +443,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_drain(full_bar(s), par);
       }
     }
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- UMMA issuer
+  } else if (warp == 1 && lane == 0 && rank == 0) {
+    // ---------------- UMMA issuer (a pair's even CTA issues for both)
     // Four MMAs per stage, each over 32 bytes of K (16 bf16 or 8 TF32 elements).
-    constexpr uint32_t idesc_full = TF32 ? idesc_tf32_f32(BM, BN) : idesc_bf16_f32(BM, BN, false);
-    constexpr uint32_t idesc_half = TF32 ? idesc_tf32_f32(BM, BN / 2) : idesc_bf16_f32(BM, BN / 2, false);
+    constexpr uint32_t idesc_full = TF32 ? idesc_tf32_f32(BM, BN) : idesc_bf16_f32(TM, BN, false);
+    constexpr uint32_t idesc_half = TF32 ? idesc_tf32_f32(BM, BN / 2) : idesc_bf16_f32(TM, BN / 2, false);
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
@@ -336,7 +456,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc = half < 0 ? idesc_full : idesc_half;
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
-      if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, wc, 2)) break;
+      const bool freed = PAIR ? mbar_wait_cluster(tempty_bar(acc), acc_phase ^ 1u, wc, 2)
+                              : mbar_wait(tempty_bar(acc), acc_phase ^ 1u, wc, 2);
+      if (!freed) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * BN;
       for (int kb = 0; kb < k_blocks; ++kb) {
@@ -349,16 +471,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t ad = sdesc_sw128(a_base + k * 32, 16, 1024);
           const uint64_t bd = sdesc_sw128(b_base + k * 32, 16, 1024);
           if constexpr (TF32) umma_tf32_ss(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+          else if constexpr (PAIR) umma_bf16_ss_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
           else umma_bf16_ss(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
         }
-        umma_commit(empty_bar(stage));
+        if constexpr (PAIR) umma_commit_pair(empty_bar(stage), 0x3);  // both CTAs' stage is free
+        else umma_commit(empty_bar(stage));
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
-      umma_commit(tfull_bar(acc));
+      if constexpr (PAIR) umma_commit_pair(tfull_bar(acc), 0x3);
+      else umma_commit(tfull_bar(acc));
     }
     // Every UMMA issued by this thread completes before TMEM is released.
-    umma_commit(drain_bar);
+    if constexpr (PAIR) umma_commit_pair(drain_bar, 0x1);
+    else umma_commit(drain_bar);
     mbar_wait_drain(drain_bar, 0);
   } else if (warp >= 2) {
     // ---------------- epilogue: TMEM -> registers -> shared -> global
@@ -371,7 +497,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;
     const int col_half = (warp - 2) >> 2;
     const uint32_t stage = smem_u32(smem + STAGES * C::STAGE_BYTES) + (warp - 2) * C::EPI_STAGE_BYTES;
-    auto row0_of = [&](int t) { return tile_m(t) * BM + quad * 32; };
+    auto row0_of = [&](int t) { return tile_m(t) * TM + static_cast<int>(rank) * BM + quad * 32; };
+    // the barrier that frees an accumulator lives in the issuing CTA (the pair's even one)
+    auto release_acc = [&](int a) {
+      if constexpr (PAIR) mbar_arrive_cluster(map_to_rank(tempty_bar(a), 0));
+      else mbar_arrive(tempty_bar(a));
+    };
     auto col_of = [&](int t) { return tile_n(t) * BN + col_half * (BN / 2); };
     float4 rb[2][8];
     constexpr bool kRowInput = (EPI == 2 || EPI == 3 || EPI == 7);  // residual rows or table rows
@@ -436,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!active(half)) {
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(tempty_bar(acc));
+        if (lane == 0) release_acc(acc);
         continue;
       }
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN +
@@ -449,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (c == CH - 1) {
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(tempty_bar(acc));
+          if (lane == 0) release_acc(acc);
         }
         epilogue_chunk<EPI, TF32>(r, stage, lane, grow0, M, N, c0 + c * 32, bias, rb[c & 1], out, row_period, ex, rs,
                                   c);
@@ -478,10 +609,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) {
+    // neither CTA frees its TMEM or shared memory while the other may still reach into them
+    __syncwarp();
+    cluster_sync_all();
+  } else {
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::TMEM_COLS);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    else tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
 }
 
@@ -490,7 +628,7 @@ cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmW, const CUt
                        int K, const float* bias, const float* resid, void* out, uint32_t* err, int num_sms,
                        cudaStream_t stream, int row_period, const wenc_host::GemmExtra& ex) {
   using C = GemmCfg<BN>;
-  auto kern = gemm_tc_kernel<BN, EPI, TF32>;
+  auto kern = gemm_tc_kernel<BN, EPI, TF32, false>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -511,6 +649,69 @@ cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmW, const CUt
   if (halves && tiles < num_sms) grid = 2 * tiles;
   return wenc_host::launch_pdl(kern, dim3(grid), dim3(kThreads), C::SMEM, stream, tmA, tmW, tmW_half ? *tmW_half : tmW,
                                tmW_half ? 1 : 0, M, N, K, bias, resid, out, err, row_period, ex, halves);
+}
+
+// The CTA-pair form: clusters of two CTAs, as many pairs as fit at once (at most one CTA per
+// SM), each walking 256-row tiles. tmW_half is W with a box of 128 rows (one CTA's half of W).
+template <int EPI>
+cudaError_t launch_pair(const CUtensorMap& tmA, const CUtensorMap& tmW_half, int M, int N, int K, const float* bias,
+                        const float* resid, void* out, uint32_t* err, int num_sms, cudaStream_t stream,
+                        int row_period, const wenc_host::GemmExtra& ex) {
+  using C = GemmCfg<256, true>;
+  auto kern = gemm_tc_kernel<256, EPI, false, true>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  // Shared-memory opt-in and the number of co-resident pairs, once per device and
+  // instantiation (a repeat by a racing host thread is harmless).
+  static std::atomic<int> max_pairs[64];
+  int pairs_fit = max_pairs[dev].load(std::memory_order_acquire);
+  if (pairs_fit <= 0) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM));
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(2 * (num_sms / 2));
+    cfg.numAttrs = 1;
+    e = cudaOccupancyMaxActiveClusters(&pairs_fit, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (pairs_fit <= 0) return cudaErrorInvalidConfiguration;
+    max_pairs[dev].store(pairs_fit, std::memory_order_release);
+  }
+  const int tiles = ((M + 255) / 256) * (N / 256);
+  const int max_units = pairs_fit < num_sms / 2 ? pairs_fit : num_sms / 2;
+  if (max_units <= 0) return cudaErrorInvalidConfiguration;
+  int pairs = tiles < max_units ? tiles : max_units;
+  // As for single CTAs: a last partial wave that would leave at least half of the pairs idle
+  // runs as twice as many half-width units.
+  const int n_tail = tiles < max_units ? tiles : tiles % max_units;
+  const int halves = (n_tail > 0 && 2 * n_tail <= max_units) ? 1 : 0;
+  if (halves && tiles < max_units) pairs = 2 * tiles;
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, tmA, tmW_half, tmW_half, 1, M, N, K, bias, resid, out, err, row_period, ex,
+                            halves);
+}
+
+// CTA pairs serve the bf16 256-column GEMMs that come with a half-height W map; the
+// environment variable WENC_GEMM_PAIR=0 keeps them on single CTAs (for comparisons).
+bool use_pair(bool tf32, int bn, int epilogue, const CUtensorMap* tmW_half) {
+  static const bool enabled = [] {
+    const char* v = getenv("WENC_GEMM_PAIR");
+    return !(v && v[0] == '0');
+  }();
+  return enabled && !tf32 && bn == 256 && tmW_half != nullptr && epilogue != 4;
 }
 
 }  // namespace
@@ -534,6 +735,17 @@ cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmW, int M, i
   if (epilogue == 7 && (!ex.copy || !ex.stats_out || ex.seg_w != bn / 2 || tf32)) return cudaErrorInvalidValue;
   if (epilogue == 3 && row_period <= 0) return cudaErrorInvalidValue;
   if (epilogue == 4 && (row_period <= 0 || row_period % 32 != 0 || N % row_period != 0)) return cudaErrorInvalidValue;
+  if (use_pair(tf32, bn, epilogue, tmW_half)) {
+    switch (epilogue) {
+      case 0: return launch_pair<0>(tmA, *tmW_half, M, N, K, bias, resid, out, err, num_sms, stream, row_period, ex);
+      case 1: return launch_pair<1>(tmA, *tmW_half, M, N, K, bias, resid, out, err, num_sms, stream, row_period, ex);
+      case 2: return launch_pair<2>(tmA, *tmW_half, M, N, K, bias, resid, out, err, num_sms, stream, row_period, ex);
+      case 3: return launch_pair<3>(tmA, *tmW_half, M, N, K, bias, resid, out, err, num_sms, stream, row_period, ex);
+      case 5: return launch_pair<5>(tmA, *tmW_half, M, N, K, bias, resid, out, err, num_sms, stream, row_period, ex);
+      case 7: return launch_pair<7>(tmA, *tmW_half, M, N, K, bias, resid, out, err, num_sms, stream, row_period, ex);
+      default: break;
+    }
+  }
 #define WENC_GEMM_CASE(BNV, EPIV, TF) \
   if (bn == BNV && epilogue == EPIV && tf32 == TF)                                        \
     return launch_one<BNV, EPIV, TF>(tmA, tmW, tmW_half, M, N, K, bias, resid, out, err, num_sms, stream, row_period, ex);
