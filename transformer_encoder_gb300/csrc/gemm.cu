@@ -20,6 +20,9 @@
 // allocates TMEM and one of its threads issues tcgen05.mma (128 x BN x 16, bf16 in, fp32
 // accumulate) into one of two TMEM accumulators; warps 2-9 drain the other accumulator
 // (tcgen05.ld -> bias / GELU / residual -> global) while the next tile is being computed.
+// The bf16 256-column GEMMs run the same roles on CTA pairs (clusters of two): a pair walks
+// 256 x 256 tiles, its even CTA issuing M256 MMAs (cta_group::2) over both CTAs' shared memory,
+// each CTA holding half of the W tile, so that six stages fit where four did.
 #include <cuda_bf16.h>
 #include <stdlib.h>
 
