@@ -30,6 +30,10 @@
  *  - Device-side waits are bounded (about one second); a wait that runs out records
  *    WENC_ERR_DEVICE_TIMEOUT in a device error word instead of hanging the GPU. It is
  *    reported by wenc_sync_status() and by the next wenc_forward* call on that handle.
+ *  - The bf16 contractions with output widths that are multiples of 256 run on pairs of SMs
+ *    (thread-block clusters of two). Setting the environment variable WENC_GEMM_PAIR=0 before
+ *    the first call keeps them on single SMs. The results are the same bits either way; the
+ *    variable exists for performance comparisons.
  */
 #ifndef WENC_H
 #define WENC_H

@@ -94,7 +94,9 @@ constexpr int kEpiResidStats = 7;
 // row_period: out[(col / P) * M * P + row * P + col % P]. P % 32 == 0 and N % P == 0.
 constexpr int kEpiBiasPlanes = 4;
 // tmW_half (optional): the same W with a box of bn / 2 rows, which the half-width units of a
-// split last wave load instead of full-height tiles.
+// split last wave load instead of full-height tiles. With it, bf16 launches with bn = 256 (other
+// than epilogue 4) run on CTA pairs: 256 x 256 tiles, each CTA of a pair loading 128 rows of A and
+// bn / 2 rows of W through tmW_half (unless WENC_GEMM_PAIR=0 in the environment).
 cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmW, int M, int N, int K, int bn, int epilogue,
                         const float* bias, const float* resid, void* out, uint32_t* err, int num_sms,
                         cudaStream_t stream, bool tf32 = false, int row_period = 0, const GemmExtra& ex = GemmExtra(),
