@@ -294,6 +294,18 @@ WENC_API wenc_status wenc_attention_tf32(const float* q, const float* k, const f
  * usable. Stream-ordered; read the outcome with wenc_sync_status(NULL). */
 WENC_API wenc_status wenc_selftest_wait_timeout(wenc_stream_t stream);
 
+/* wenc_selftest_gemm_schedule -- host only, no device work: replays how a contraction of
+ * M x N output elements divides its tiles among the units of one launch (single CTAs on
+ * 128-row tiles when pair is 0, CTA pairs on 256 x 256 tiles when pair is 1), through the same
+ * schedule code the GEMM kernel runs, for a launch of at most max_units units (the SM count, or
+ * the number of pairs that fit). cover[2t + h] counts how often column half h of tile t is
+ * computed (cover_len >= 2 x tiles); unit_halves[u] (max_units entries, may be NULL) is the
+ * number of half tiles unit u computes; *units and *halves receive the launch size and whether
+ * its last wave runs as half-width units. Returns WENC_ERR_INVALID_ARG for an unsupported
+ * shape or a short cover array. */
+WENC_API wenc_status wenc_selftest_gemm_schedule(int M, int N, int pair, int max_units, int* cover, int cover_len,
+                                                 int* unit_halves, int* units, int* halves);
+
 /* wenc_sync_status -- synchronise the device and read the device error word of `h`
  * (or, when h is NULL, the word shared by the handle-less entry points), clearing it.
  * Returns WENC_OK, WENC_ERR_DEVICE_TIMEOUT or WENC_ERR_CUDA. */

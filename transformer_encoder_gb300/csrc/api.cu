@@ -1005,6 +1005,18 @@ wenc_status wenc_selftest_wait_timeout(wenc_stream_t stream) {
   return WENC_OK;
 }
 
+wenc_status wenc_selftest_gemm_schedule(int M, int N, int pair, int max_units, int* cover, int cover_len,
+                                        int* unit_halves, int* units, int* halves) {
+  g_last_error.clear();
+  if (!cover || !units || !halves) return fail(WENC_ERR_INVALID_ARG, "cover/units/halves is NULL");
+  const int r = wenc_host::gemm_schedule_cover(M, N, pair != 0, max_units, cover, cover_len, unit_halves, units,
+                                               halves);
+  if (r == -1) return fail(WENC_ERR_INVALID_ARG, "shape %d x %d (pair %d, %d units) unsupported or cover too short", M,
+                           N, pair, max_units);
+  if (r != 0) return fail(WENC_ERR_INVALID_ARG, "schedule produced a tile outside the launch");
+  return WENC_OK;
+}
+
 wenc_status wenc_sync_status(wenc* h) {
   g_last_error.clear();
   cudaError_t e = cudaDeviceSynchronize();

@@ -279,6 +279,55 @@ __device__ __forceinline__ void epilogue_chunk(const uint32_t (&acc)[32], uint32
   __syncwarp();  // the stage is rewritten by the next chunk
 }
 
+// How one launch divides its output tiles among its scheduling units (CTAs, or CTA pairs), the
+// same sequence for every role of a unit: whole tiles unit + i G (G = the number of units) over
+// the first n_dp tiles; then, when the launch splits its last partial wave (tail_halves), one
+// half-width unit each: the n_tail = num_tiles % G remaining tiles become 2 n_tail units of
+// BN / 2 columns (an M128 (pair: M256) N(BN/2) product over the whole K), unit u < 2 n_tail
+// taking half u % 2 of tile n_dp + u / 2. Each output element is the same fixed-order dot product
+// either way. The kernel and the host-side self-test run this same code.
+struct TileSchedule {
+  int unit, n_units, n_dp, n_mine;
+  bool has_unit;
+  __host__ __device__ TileSchedule(int num_tiles, int unit_, int n_units_, bool tail_halves)
+      : unit(unit_), n_units(n_units_) {
+    const int n_tail = tail_halves ? num_tiles % n_units : 0;
+    n_dp = num_tiles - n_tail;
+    n_mine = (unit < n_dp) ? (n_dp - 1 - unit) / n_units + 1 : 0;
+    has_unit = unit < 2 * n_tail;
+  }
+  // item i of this unit: its tile and, for the half-width unit, which half (-1: the whole tile)
+  __host__ __device__ bool item(int i, int& tile, int& half) const {
+    if (i < n_mine) {
+      tile = unit + i * n_units;
+      half = -1;
+      return true;
+    }
+    if (i == n_mine && has_unit) {
+      tile = n_dp + unit / 2;
+      half = unit % 2;
+      return true;
+    }
+    return false;
+  }
+};
+
+// The size of a launch: one unit per tile, at most max_units; a last partial wave that would
+// leave at least half of the units idle runs as twice as many half-width units (all tiles, when
+// there are at most half as many tiles as units).
+struct LaunchPlan {
+  int units;
+  int halves;
+};
+inline LaunchPlan plan_launch(int tiles, int max_units) {
+  LaunchPlan p;
+  p.units = tiles < max_units ? tiles : max_units;
+  const int n_tail = tiles < max_units ? tiles : tiles % max_units;
+  p.halves = (n_tail > 0 && 2 * n_tail <= max_units) ? 1 : 0;
+  if (p.halves && tiles < max_units) p.units = 2 * tiles;
+  return p;
+}
+
 template <int BN, int EPI, bool TF32, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
@@ -335,30 +384,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   constexpr int BKE = TF32 ? 32 : BK;  // K elements per stage (128-byte rows)
   const int k_blocks = K / BKE;
-  // Work items of this unit (CTA or pair), the same sequence for every role: whole tiles
-  // unit + i G (G = the number of units) over the first n_dp tiles; then, when the launch splits
-  // its last partial wave (tail_halves), one half-width unit: the n_tail = num_tiles % G
-  // remaining tiles become 2 n_tail units of BN / 2 columns (an M128 (pair: M256) N(BN/2)
-  // product over the whole K), unit u < 2 n_tail taking half u % 2 of tile n_dp + u / 2. Each
-  // output element is the same fixed-order dot product either way.
-  const int n_tail = tail_halves ? num_tiles % n_units : 0;
-  const int n_dp = num_tiles - n_tail;
-  const int n_mine = (unit < n_dp) ? (n_dp - 1 - unit) / n_units + 1 : 0;
-  const bool has_unit = unit < 2 * n_tail;
-  // item i of this unit: its tile and, for the half-width unit, which half (-1: the whole tile)
-  auto item = [&](int i, int& tile, int& half) -> bool {
-    if (i < n_mine) {
-      tile = unit + i * n_units;
-      half = -1;
-      return true;
-    }
-    if (i == n_mine && has_unit) {
-      tile = n_dp + unit / 2;
-      half = unit % 2;
-      return true;
-    }
-    return false;
-  };
+  // Work items of this unit (see TileSchedule)
+  const TileSchedule sched(num_tiles, unit, n_units, tail_halves != 0);
+  auto item = [&](int i, int& tile, int& half) -> bool { return sched.item(i, tile, half); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -643,15 +671,10 @@ cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmW, const CUt
     if (e != cudaSuccess) return e;
     configured_device.store(dev, std::memory_order_release);
   }
-  const int tiles = ((M + BM - 1) / BM) * (N / BN);
-  int grid = tiles < num_sms ? tiles : num_sms;
-  // The last partial wave, when it would leave at least half of the SMs idle, runs as twice as
-  // many half-width units (all tiles, when there are fewer than half as many as SMs).
-  const int n_tail = tiles < num_sms ? tiles : tiles % num_sms;
-  const int halves = (n_tail > 0 && 2 * n_tail <= num_sms) ? 1 : 0;
-  if (halves && tiles < num_sms) grid = 2 * tiles;
-  return wenc_host::launch_pdl(kern, dim3(grid), dim3(kThreads), C::SMEM, stream, tmA, tmW, tmW_half ? *tmW_half : tmW,
-                               tmW_half ? 1 : 0, M, N, K, bias, resid, out, err, row_period, ex, halves);
+  const LaunchPlan plan = plan_launch(((M + BM - 1) / BM) * (N / BN), num_sms);
+  return wenc_host::launch_pdl(kern, dim3(plan.units), dim3(kThreads), C::SMEM, stream, tmA, tmW,
+                               tmW_half ? *tmW_half : tmW, tmW_half ? 1 : 0, M, N, K, bias, resid, out, err,
+                               row_period, ex, plan.halves);
 }
 
 // The CTA-pair form: clusters of two CTAs, as many pairs as fit at once (at most one CTA per
@@ -692,19 +715,13 @@ cudaError_t launch_pair(const CUtensorMap& tmA, const CUtensorMap& tmW_half, int
     if (pairs_fit <= 0) return cudaErrorInvalidConfiguration;
     max_pairs[dev].store(pairs_fit, std::memory_order_release);
   }
-  const int tiles = ((M + 255) / 256) * (N / 256);
   const int max_units = pairs_fit < num_sms / 2 ? pairs_fit : num_sms / 2;
   if (max_units <= 0) return cudaErrorInvalidConfiguration;
-  int pairs = tiles < max_units ? tiles : max_units;
-  // As for single CTAs: a last partial wave that would leave at least half of the pairs idle
-  // runs as twice as many half-width units.
-  const int n_tail = tiles < max_units ? tiles : tiles % max_units;
-  const int halves = (n_tail > 0 && 2 * n_tail <= max_units) ? 1 : 0;
-  if (halves && tiles < max_units) pairs = 2 * tiles;
-  cfg.gridDim = dim3(2 * pairs);
+  const LaunchPlan plan = plan_launch(((M + 255) / 256) * (N / 256), max_units);
+  cfg.gridDim = dim3(2 * plan.units);
   cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, tmA, tmW_half, tmW_half, 1, M, N, K, bias, resid, out, err, row_period, ex,
-                            halves);
+                            plan.halves);
 }
 
 // CTA pairs serve the bf16 256-column GEMMs that come with a half-height W map; the
@@ -720,6 +737,37 @@ bool use_pair(bool tf32, int bn, int epilogue, const CUtensorMap* tmW_half) {
 }  // namespace
 
 namespace wenc_host {
+
+int gemm_schedule_cover(int M, int N, bool pair, int max_units, int* cover, int cover_len, int* unit_halves,
+                        int* units_out, int* halves_out) {
+  const int bn = pair ? 256 : gemm_pick_bn(N);
+  if (M < 1 || bn == 0 || N % bn != 0 || max_units < 1) return -1;
+  const int rows = pair ? 2 * BM : BM;
+  const long long tiles_ll = static_cast<long long>((M + rows - 1) / rows) * (N / bn);
+  if (tiles_ll > cover_len / 2) return -1;
+  const int tiles = static_cast<int>(tiles_ll);
+  const LaunchPlan plan = plan_launch(tiles, max_units);
+  for (int i = 0; i < 2 * tiles; ++i) cover[i] = 0;
+  for (int u = 0; u < plan.units; ++u) {
+    const TileSchedule sched(tiles, u, plan.units, plan.halves != 0);
+    int n = 0, tile, half;
+    for (int i = 0; sched.item(i, tile, half); ++i) {
+      if (tile < 0 || tile >= tiles) return -2;
+      if (half < 0) {
+        ++cover[2 * tile];
+        ++cover[2 * tile + 1];
+        n += 2;
+      } else {
+        ++cover[2 * tile + half];
+        n += 1;
+      }
+    }
+    if (unit_halves) unit_halves[u] = n;
+  }
+  *units_out = plan.units;
+  *halves_out = plan.halves;
+  return 0;
+}
 
 int gemm_pick_bn(int N) {
   if (N % 256 == 0) return 256;

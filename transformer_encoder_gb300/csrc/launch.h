@@ -63,6 +63,13 @@ cudaError_t launch_fold_ln(const void* w, bool w_bf16, const float* ln_w, const 
 // C[M, N] = A[M, K] * W[N, K]^T with a fused epilogue (wenc_epilogue values).
 // Tile: 128 x bn (bn = 256 or 128), k-block 64. tmA: box 64 x 128 over A; tmW: box 64 x bn over W.
 int gemm_pick_bn(int N);  // 0 if N is unsupported
+// Host-side replay of how a launch of M x N (single CTAs: 128-row tiles of gemm_pick_bn(N)
+// columns; pair: 256 x 256 tiles) with at most max_units units divides its tiles, through the
+// same schedule code the kernel runs. cover[2t + h] (cover_len >= 2 x tiles) counts how often
+// column half h of tile t is computed; unit_halves[u] (max_units entries, or NULL) the half-tiles
+// unit u computes. Returns 0, or < 0 for an unsupported shape or a short cover array.
+int gemm_schedule_cover(int M, int N, bool pair, int max_units, int* cover, int cover_len, int* unit_halves,
+                        int* units_out, int* halves_out);
 constexpr int kGemmBM = 128;
 constexpr int kGemmBK = 64;
 // tf32 = false: bf16 A and W (maps with box 64 x rows), epilogues 0, 1, 2.

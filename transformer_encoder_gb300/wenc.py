@@ -32,7 +32,7 @@ EXPORTED_SYMBOLS = (
     "wenc_attention", "wenc_layernorm", "wenc_linear", "wenc_sync_status", "wenc_destroy", "wenc_last_error",
     "wenc_version", "wenc_selftest_wait_timeout", "wenc_attention_static", "wenc_attention_static_capacity",
     "wenc_linear_tf32", "wenc_attention_tf32", "wenc_set_stem", "wenc_stem", "wenc_encode", "wenc_encode_launches",
-    "wenc_set_cross_kv", "wenc_cross_kv",
+    "wenc_set_cross_kv", "wenc_cross_kv", "wenc_selftest_gemm_schedule",
 )
 
 
@@ -92,6 +92,8 @@ def lib() -> ctypes.CDLL:
         L.wenc_attention_tf32.argtypes = [vp, vp, vp, vp, i, i, i, i, vp]
         L.wenc_sync_status.argtypes = [vp]
         L.wenc_selftest_wait_timeout.argtypes = [vp]
+        ip = ctypes.POINTER(ctypes.c_int)
+        L.wenc_selftest_gemm_schedule.argtypes = [i, i, i, i, ip, i, ip, ip, ip]
         L.wenc_attention_static.argtypes = [vp, vp, vp, vp, i, i, i, i, vp]
         L.wenc_attention_static.restype = ctypes.c_int
         L.wenc_attention_static_capacity.argtypes = []
@@ -103,7 +105,8 @@ def lib() -> ctypes.CDLL:
         for name in ("wenc_create", "wenc_forward", "wenc_forward_layers", "wenc_set_launch_events", "wenc_attention",
                      "wenc_layernorm", "wenc_linear", "wenc_sync_status", "wenc_forward_launches",
                      "wenc_selftest_wait_timeout", "wenc_linear_tf32", "wenc_attention_tf32", "wenc_set_stem",
-                     "wenc_stem", "wenc_encode", "wenc_encode_launches", "wenc_set_cross_kv", "wenc_cross_kv"):
+                     "wenc_stem", "wenc_encode", "wenc_encode_launches", "wenc_set_cross_kv", "wenc_cross_kv",
+                     "wenc_selftest_gemm_schedule"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -374,6 +377,25 @@ def attention_tf32(q, k, v, out=None, stream=None):
 def selftest_wait_timeout(stream=None):
     """Launch the bounded-wait self-test (returns immediately; read it with sync_status())."""
     _check(lib().wenc_selftest_wait_timeout(_stream(stream)))
+
+
+def gemm_schedule(M: int, N: int, pair: bool, max_units: int):
+    """Host-only replay of a GEMM launch's tile schedule (see wenc_selftest_gemm_schedule).
+
+    Returns (cover, unit_halves, units, halves): cover[t, h] = how often column half h of tile t
+    is computed, unit_halves[u] = half tiles computed by unit u (u < units)."""
+    import numpy as np
+    rows = 256 if pair else 128
+    bn = 256 if pair or N % 256 == 0 else 128
+    tiles = -(-M // rows) * (N // bn)
+    cover = (ctypes.c_int * max(2 * tiles, 2))()
+    unit_halves = (ctypes.c_int * max_units)()
+    units, halves = ctypes.c_int(), ctypes.c_int()
+    _check(lib().wenc_selftest_gemm_schedule(M, N, int(pair), max_units, cover, len(cover), unit_halves,
+                                             ctypes.byref(units), ctypes.byref(halves)))
+    cov = np.frombuffer(cover, dtype=np.int32, count=2 * tiles).reshape(tiles, 2).copy()
+    work = np.frombuffer(unit_halves, dtype=np.int32, count=units.value).copy()
+    return cov, work, units.value, halves.value
 
 
 def sync_status(encoder: Encoder | None = None):
