@@ -433,13 +433,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int tile, half;
     for (int i = 0; ok && item(i, tile, half); ++i) {
-      // A pair's CTA loads its own 128 rows of A and its share of W (BN / 2 rows through the
-      // half-box map; BN / 4 of them in a half-width unit, the other rows of the box unused),
-      // counted on the even CTA's full barrier, which expects both CTAs' bytes.
+      // First A row and first W row of this CTA's loads. Single CTA: a whole tile loads BN rows of
+      // W; a half-width unit BN / 2 rows through the half-box map (without one, BN rows from its
+      // half's first column, rows past N reading as zeros, of which it multiplies the first
+      // BN / 2). CTA pair: each CTA loads its own 128 rows of A and its share of W through the
+      // half-box map (BN / 2 rows; BN / 4 of them in a half-width unit, the rest of the box
+      // unused), counted on the even CTA's full barrier, which expects both CTAs' bytes.
       const int m0 = tile_m(tile) * TM + static_cast<int>(rank) * BM;
-      // a half-width unit loads BN / 2 rows of W through the half-box map (or, without one, the
-      // BN rows from its half's first column, rows past N reading as zeros) and multiplies the
-      // first BN / 2 of them
       const int n0 = tile_n(tile) * BN + (half > 0 ? BN / 2 : 0) +
                      (PAIR ? static_cast<int>(rank) * (half < 0 ? BN / 2 : BN / 4) : 0);
       const bool hb = half >= 0 && half_box;
