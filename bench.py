@@ -23,7 +23,8 @@ encoder output, not the K/V planes, which a decoder consumes on the device.
 roofline peak is the measured bf16 peak times the nominal TF32/BF16 ratio (1.1 / 2.25 PFLOP/s).
 
 `--impl reference` times the f64 CPU oracle (the only other implementation) on the host
-cores on a bounded sample of the same workload (one block of one window per step) and
+cores on a bounded sample of the same workload (one block of one window per step, plus that
+window's stem with `--stem` and two decoder layers' cross K/V with `--cross-kv`) and
 extrapolates to windows/s.
 """
 from __future__ import annotations
@@ -268,17 +269,31 @@ def run_reference(args, w):
     rank, _, world = dist_env()
     if rank != 0:
         return 0
-    times = time_oracle_block(w, 0.0, steps=args.warmup)  # warm-up (untimed)
-    times = time_oracle_block(w, 0.0, steps=args.steps)
-    total = sum(times)
-    win_s = args.steps / (total * w.n_layers)
+    # Each step: one block of one window (x n_layers), plus, with --stem, the stem of that window
+    # and, with --cross-kv, the cross K/V of two decoder layers (x n_layers / 2): the work of one
+    # window of the wenc arm's step, extrapolated from a bounded sample.
+    def step_seconds():
+        t = time_oracle_block(w, 0.0, steps=1)[0] * w.n_layers
+        if args.stem:
+            t += time_oracle_stem(w, 1)[0]
+        if args.cross_kv:
+            t += time_oracle_cross(w, 2) * w.n_layers / 2
+        return t
+
+    for _ in range(args.warmup):  # warm-up (untimed)
+        step_seconds()
+    total = sum(step_seconds() for _ in range(args.steps))
+    win_s = args.steps / total
+    extra = (" + the convolutional stem" if args.stem else "") + \
+            (f" + cross K/V of 2 decoder layers x{w.n_layers / 2:g}" if args.cross_kv else "")
+    sample = f"one block of one window per step at {w.name} dims, x{w.n_layers} blocks{extra}"
     line = {
         "impl": "reference", "metric": METRIC, "value": win_s, "unit": "windows/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": workload_desc(w), "sample": "one block of one window per step, extrapolated"},
+        "config": {"workload": workload_desc(w) + extra, "sample": sample + ", extrapolated"},
         "cpu_baseline": {"value": win_s, "unit": "windows/s", "cores": host_cores(), "kind": "oracle",
-                         "sample": f"one block of one window per step at {w.name} dims, x{w.n_layers} blocks"},
+                         "sample": sample},
         "e2e": {"value": win_s, "unit": "windows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

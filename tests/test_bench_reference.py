@@ -48,3 +48,15 @@ def test_reference_line_keeps_the_contract(monkeypatch):
 def test_reference_runs_on_rank_zero_only(monkeypatch):
     rc, lines = _run(monkeypatch, rank=1, world=2)
     assert rc == 0 and lines == []
+
+
+def test_reference_times_the_stem_and_cross_kv_when_asked(monkeypatch):
+    monkeypatch.setattr(sys, "argv", ["bench.py"])
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        rc = bench.main(ARGS + ["--stem", "--cross-kv"])
+    lines = [l for l in buf.getvalue().splitlines() if l.strip()]
+    assert rc == 0 and len(lines) == 1
+    d = json.loads(lines[0])
+    assert "stem" in d["config"]["workload"] and "cross K/V" in d["config"]["workload"]
+    assert "stem" in d["cpu_baseline"]["sample"] and d["value"] > 0
