@@ -294,6 +294,20 @@ WENC_API wenc_status wenc_attention_tf32(const float* q, const float* k, const f
  * usable. Stream-ordered; read the outcome with wenc_sync_status(NULL). */
 WENC_API wenc_status wenc_selftest_wait_timeout(wenc_stream_t stream);
 
+/* wenc_selftest_gemm_pair_abort -- exercises the failure path of the CTA-pair GEMM (the pages
+ * have no counterpart). Runs out = bf16(A W^T + bias) (A bf16 [M, K], W bf16 [N, K], bias f32
+ * [N], out bf16 [M, N], device pointers, 16-byte aligned; N a multiple of 256, K of 64) on CTA
+ * pairs, with the odd CTA of every pair giving up after `stop_after` k-block stages as if one of
+ * its waits had run out. The even CTA's waits for the missing data then run out too (about a
+ * second); the pair drains every copy that may be in flight, in order, before either CTA
+ * exits, and WENC_ERR_DEVICE_TIMEOUT is recorded (site 31, or the site of the even CTA's wait)
+ * in the handle-less device error word; no trap, the context stays usable and `out` holds no
+ * defined values. Stream-ordered; read the outcome with wenc_sync_status(NULL).
+ * WENC_ERR_UNSUPPORTED when the CTA-pair form is switched off (WENC_GEMM_PAIR=0). */
+WENC_API wenc_status wenc_selftest_gemm_pair_abort(const uint16_t* A, const uint16_t* W, const float* bias,
+                                                   uint16_t* out, int M, int N, int K, int stop_after,
+                                                   wenc_stream_t stream);
+
 /* wenc_selftest_gemm_schedule -- host only, no device work: replays how a contraction of
  * M x N output elements divides its tiles among the units of one launch (single CTAs on
  * 128-row tiles when pair is 0, CTA pairs on 256 x 256 tiles when pair is 1), through the same

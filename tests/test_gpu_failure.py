@@ -1,4 +1,4 @@
-"""Failure detection on the GPU without a fault: a bounded wait runs out and is reported.
+"""Failure detection on the GPU without a fault: bounded waits run out and are reported.
 
 The self-test kernel waits on an mbarrier that nothing arrives on, with the same bounded
 wait every kernel of the library uses. The wait must give up after about a second, record
@@ -35,4 +35,36 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     torch.cuda.synchronize()
     f = lambda a: synth.bf16_bits_to_f32(a).reshape(1, 300, 128)
     attention_gate(bf16_to_f64(out).reshape(1, 300, 128), f(q), f(k), f(v), 2, what="after the timeout")
+    sync_status()
+
+
+@pytest.mark.parametrize("stop_after", [0, 3])
+def test_cta_pair_gemm_abort_drains_and_context_survives(stop_after):
+    """The odd CTA of every pair gives up after `stop_after` k-blocks; the even CTA's waits then
+    run out, the pair drains its copies in order and both CTAs exit: the status reads
+    DEVICE_TIMEOUT within a few seconds and the same GEMM, run normally next, is correct."""
+    import torch
+
+    import oracle
+    from transformer_encoder_gb300 import WencError, linear, selftest_gemm_pair_abort, sync_status
+    sync_status()
+    M, N, K = 1000, 512, 1280  # 4 x 2 pair tiles (fewer than the pairs of a GB300), 20 k-blocks
+    rng = np.random.default_rng(31 + stop_after)
+    a = synth.round_to_bf16(rng.standard_normal((M, K)).astype(np.float32))
+    wt = synth.round_to_bf16((0.05 * rng.standard_normal((N, K))).astype(np.float32))
+    bias = (0.1 * rng.standard_normal(N)).astype(np.float32)
+    ta = torch.from_numpy(a).cuda().to(torch.bfloat16)
+    tw = torch.from_numpy(wt).cuda().to(torch.bfloat16)
+    tb = torch.from_numpy(bias).cuda()
+    t0 = time.time()
+    selftest_gemm_pair_abort(ta, tw, tb, stop_after)
+    with pytest.raises(WencError, match="DEVICE_TIMEOUT"):
+        sync_status()
+    assert time.time() - t0 < 30.0
+    sync_status()  # the word was cleared by the read
+    out = linear(ta, tw, tb)
+    torch.cuda.synchronize()
+    ref = oracle.linear(a, wt, bias)
+    got = bf16_to_f64(out)
+    assert (np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 2e-5 * np.sqrt(np.mean(ref * ref))).all()
     sync_status()

@@ -430,6 +430,7 @@ void enqueue_blocks(wenc* h, const float* in, float* out, int B, int first, int 
 
 // Helpers shared with the other entry-point files (status message, error word, device checks).
 wenc_status wenc_internal_fail(wenc_status s, const char* msg) { return fail(s, "%s", msg); }
+void wenc_internal_clear_error() { g_last_error.clear(); }
 uint32_t* wenc_internal_error_word(std::string* why) { return global_error_word(why); }
 bool wenc_internal_is_sm103(std::string* why) { return device_is_sm103(why); }
 int wenc_internal_sm_count() { return sm_count(); }
@@ -1001,6 +1002,33 @@ wenc_status wenc_selftest_wait_timeout(wenc_stream_t stream) {
   if (!err) return fail(WENC_ERR_CUDA, "%s", why.c_str());
   stall_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(err);
   cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  return WENC_OK;
+}
+
+wenc_status wenc_selftest_gemm_pair_abort(const uint16_t* A, const uint16_t* W, const float* bias, uint16_t* out, int M,
+                                          int N, int K, int stop_after, wenc_stream_t stream) {
+  g_last_error.clear();
+  if (!A || !W || !bias || !out) return fail(WENC_ERR_INVALID_ARG, "A/W/bias/out is NULL");
+  if (M < 1 || stop_after < 0) return fail(WENC_ERR_INVALID_ARG, "M must be >= 1 and stop_after >= 0");
+  if (N < 256 || N % 256 != 0) return fail(WENC_ERR_UNSUPPORTED, "N %d: the CTA-pair form needs a multiple of 256", N);
+  if (K < 64 || K % 64 != 0) return fail(WENC_ERR_UNSUPPORTED, "K %d: must be a positive multiple of 64", K);
+  if (!aligned16(A) || !aligned16(W) || !aligned16(bias) || !aligned16(out))
+    return fail(WENC_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
+  std::string why;
+  if (!device_is_sm103(&why)) return fail(WENC_ERR_UNSUPPORTED, "%s", why.c_str());
+  if (!wenc_host::gemm_pair_enabled()) return fail(WENC_ERR_UNSUPPORTED, "CTA-pair GEMMs are off (WENC_GEMM_PAIR=0)");
+  uint32_t* err = global_error_word(&why);
+  if (!err) return fail(WENC_ERR_CUDA, "%s", why.c_str());
+  CUtensorMap ta, tw, tw_h;
+  bool ok = wenc_host::make_tmap_2d_bf16(&ta, A, K, M, size_t(K) * 2, 64, wenc_host::kGemmBM, &why) &&
+            wenc_host::make_tmap_2d_bf16(&tw, W, K, N, size_t(K) * 2, 64, 256, &why) &&
+            wenc_host::make_tmap_2d_bf16(&tw_h, W, K, N, size_t(K) * 2, 64, 128, &why);
+  if (!ok) return fail(WENC_ERR_INVALID_ARG, "%s", why.c_str());
+  wenc_host::GemmExtra ex;
+  ex.stop_odd_after = stop_after;
+  cudaError_t e = wenc_host::launch_gemm(ta, tw, M, N, K, 256, WENC_EPI_BIAS_BF16, bias, nullptr, out, err, sm_count(),
+                                         reinterpret_cast<cudaStream_t>(stream), false, 0, ex, &tw_h);
   if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
   return WENC_OK;
 }

@@ -52,7 +52,7 @@ struct GemmCfg {
   static constexpr uint32_t B_BYTES = (PAIR ? BN / 2 : BN) * 128;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TMEM_COLS = 2 * BN;  // two fp32 accumulators of BN columns
-  static constexpr uint32_t NUM_BARS = 2 * STAGES + 5;
+  static constexpr uint32_t NUM_BARS = 2 * STAGES + 6;
   static constexpr uint32_t EPI_STAGE_BYTES = 32 * 32 * 4;  // one warp's 32 x 32 fp32 chunk
   static constexpr uint32_t EPI_BYTES = kEpiWarps * EPI_STAGE_BYTES;
   static constexpr size_t SMEM = 1024 /*align slack*/ + STAGES * STAGE_BYTES + EPI_BYTES + NUM_BARS * 8 + 16;
@@ -105,6 +105,14 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
 }
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// Count `bytes` as arrived on this CTA's barrier without a copy (for a copy that was expected but
+// never issued).
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 // Bounded wait (as mbar_wait) that acquires at cluster scope: for barriers the peer CTA arrives on.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
@@ -348,8 +356,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  // CTA pair: the odd CTA's producer reports how many stages it loaded (into peer_loads of the
+  // even CTA, then one arrival on loads_bar), so that the even CTA can drain every copy of the
+  // pair that may still be in flight before the pair's final barrier.
+  const uint32_t loads_bar = bar0 + 8u * (2 * STAGES + 5);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
   volatile uint32_t* abort_flag = tmem_slot + 1;
+  volatile uint32_t* peer_loads = tmem_slot + 2;
   const WaitCtx wc{abort_flag, err};
 
   const int warp = threadIdx.x >> 5;
@@ -398,7 +411,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(tempty_bar(a), PAIR ? 2 * kEpiWarps : kEpiWarps);  // one arrival per epilogue warp (of the pair)
     }
     mbar_init(drain_bar, 1);
+    mbar_init(loads_bar, 1);
     *abort_flag = 0u;
+    *peer_loads = 0u;
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmW);
@@ -430,6 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     uint32_t issued_mask = 0;
+    uint32_t loads = 0;  // stages this CTA has loaded
     bool ok = true;
     int tile, half;
     for (int i = 0; ok && item(i, tile, half); ++i) {
@@ -445,6 +461,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool hb = half >= 0 && half_box;
       const uint32_t stage_bytes = hb ? C::A_BYTES + C::B_BYTES / 2 : C::STAGE_BYTES;
       for (int kb = 0; kb < k_blocks; ++kb) {
+        if (PAIR && rank != 0 && ex.stop_odd_after >= 0 && loads >= static_cast<uint32_t>(ex.stop_odd_after)) {
+          // self-test: this producer gives up here as if a wait had run out (site 31)
+          *abort_flag = 1u;
+          *reinterpret_cast<volatile uint32_t*>(err) = kErrTimeout | (31u << 8);
+          ok = false;
+          break;
+        }
         if (!mbar_wait(empty_bar(stage), phase ^ 1u, wc, 1)) { ok = false; break; }
         if constexpr (PAIR) {
           if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * C::STAGE_BYTES);
@@ -457,14 +480,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(sB + stage * C::B_BYTES, hb ? &tmWh : &tmW, full_bar(stage), kb * BKE, n0);
         }
         issued_mask |= 1u << stage;
+        ++loads;
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
     }
-    if (!ok && PAIR && rank != 0) {
-      // Error path of the odd CTA: its copies count on the even CTA's barriers; give the ones
-      // in flight time to land (they take microseconds) before the CTA exits.
-      const uint64_t t0 = global_timer_ns();
-      while (global_timer_ns() - t0 < 200000ull) {
+    if constexpr (PAIR) {
+      // Ordered drain of the pair's copies, on every exit: both CTAs' copies of a stage complete on
+      // the even CTA's full barrier, and a producer reuses a stage only after the MMAs consumed it,
+      // so the copies that may still be in flight are those of the last STAGES stages either CTA
+      // loaded. The odd CTA reports its count; the even CTA waits for each of those stages, first
+      // arming the ones only the odd CTA loaded (for the odd CTA's bytes) and cancelling the bytes
+      // the odd CTA never sent for the ones only it armed. Neither CTA leaves the final cluster
+      // barrier before this ends, so no copy lands in shared memory that has been released.
+      if (rank != 0) {
+        st_cluster_u32(map_to_rank(smem_u32(const_cast<uint32_t*>(peer_loads)), 0), loads);
+        mbar_arrive_cluster(map_to_rank(loads_bar, 0));  // release: the count is visible with the arrival
+      } else {
+        uint32_t odd = loads;
+        const uint64_t t0 = global_timer_ns();
+        bool have = false;
+        while (!(have = mbar_try_wait_cluster(loads_bar, 0)) && global_timer_ns() - t0 <= kWaitLimitNs) {
+        }
+        if (have) odd = *peer_loads;
+        const uint32_t n = loads > odd ? loads : odd;
+        for (uint32_t i = n > static_cast<uint32_t>(STAGES) ? n - STAGES : 0; i < n; ++i) {
+          const int s = static_cast<int>(i % STAGES);
+          if (i >= loads) mbar_arrive_expect_tx(full_bar(s), C::STAGE_BYTES);
+          else if (i >= odd) mbar_complete_tx(full_bar(s), C::STAGE_BYTES);
+          mbar_wait_drain(full_bar(s), (i / STAGES) & 1u);
+        }
       }
     } else if (!ok) {
       // Error path: let the copies already issued land before the CTA exits.
@@ -737,6 +781,8 @@ bool use_pair(bool tf32, int bn, int epilogue, const CUtensorMap* tmW_half) {
 }  // namespace
 
 namespace wenc_host {
+
+bool gemm_pair_enabled() { return use_pair(false, 256, 0, reinterpret_cast<const CUtensorMap*>(1)); }
 
 int gemm_schedule_cover(int M, int N, bool pair, int max_units, int* cover, int cover_len, int* unit_halves,
                         int* units_out, int* halves_out) {

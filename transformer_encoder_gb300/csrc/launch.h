@@ -63,6 +63,7 @@ cudaError_t launch_fold_ln(const void* w, bool w_bf16, const float* ln_w, const 
 // C[M, N] = A[M, K] * W[N, K]^T with a fused epilogue (wenc_epilogue values).
 // Tile: 128 x bn (bn = 256 or 128), k-block 64. tmA: box 64 x 128 over A; tmW: box 64 x bn over W.
 int gemm_pick_bn(int N);  // 0 if N is unsupported
+bool gemm_pair_enabled();   // bf16 256-column GEMMs run as CTA pairs (not switched off by WENC_GEMM_PAIR=0)
 // Host-side replay of how a launch of M x N (single CTAs: 128-row tiles of gemm_pick_bn(N)
 // columns; pair: 256 x 256 tiles) with at most max_units units divides its tiles, through the
 // same schedule code the kernel runs. cover[2t + h] (cover_len >= 2 x tiles) counts how often
@@ -93,6 +94,10 @@ struct GemmExtra {
   uint16_t* copy = nullptr;
   float eps = 0.0f;
   int seg_w = 0;
+  // Self-test only (wenc_selftest_gemm_pair_abort): in the CTA-pair form, the odd CTA's TMA
+  // producer stops after this many stages and reports a timeout, as if one of its waits had run
+  // out; -1 (every other caller) leaves the kernel unchanged.
+  int stop_odd_after = -1;
 };
 constexpr int kEpiLnBias = 5;
 constexpr int kEpiResidStats = 7;

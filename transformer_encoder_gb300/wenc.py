@@ -12,7 +12,7 @@ import os
 
 __all__ = [
     "WencError", "lib", "lib_path", "Encoder", "attention", "attention_tf32", "layernorm", "linear", "linear_tf32",
-    "sync_status", "EPI_BIAS_BF16", "EPI_BIAS_GELU_BF16", "EPI_BIAS_RESID_F32", "LN_OUT_F32", "LN_OUT_BF16",
+    "sync_status", "selftest_gemm_pair_abort", "EPI_BIAS_BF16", "EPI_BIAS_GELU_BF16", "EPI_BIAS_RESID_F32", "LN_OUT_F32", "LN_OUT_BF16",
     "LN_OUT_TF32", "PREC_BF16", "PREC_TF32", "EXPORTED_SYMBOLS",
 ]
 
@@ -32,7 +32,7 @@ EXPORTED_SYMBOLS = (
     "wenc_attention", "wenc_layernorm", "wenc_linear", "wenc_sync_status", "wenc_destroy", "wenc_last_error",
     "wenc_version", "wenc_selftest_wait_timeout", "wenc_attention_static", "wenc_attention_static_capacity",
     "wenc_linear_tf32", "wenc_attention_tf32", "wenc_set_stem", "wenc_stem", "wenc_encode", "wenc_encode_launches",
-    "wenc_set_cross_kv", "wenc_cross_kv", "wenc_selftest_gemm_schedule",
+    "wenc_set_cross_kv", "wenc_cross_kv", "wenc_selftest_gemm_schedule", "wenc_selftest_gemm_pair_abort",
 )
 
 
@@ -92,6 +92,7 @@ def lib() -> ctypes.CDLL:
         L.wenc_attention_tf32.argtypes = [vp, vp, vp, vp, i, i, i, i, vp]
         L.wenc_sync_status.argtypes = [vp]
         L.wenc_selftest_wait_timeout.argtypes = [vp]
+        L.wenc_selftest_gemm_pair_abort.argtypes = [vp, vp, vp, vp, i, i, i, i, vp]
         ip = ctypes.POINTER(ctypes.c_int)
         L.wenc_selftest_gemm_schedule.argtypes = [i, i, i, i, ip, i, ip, ip, ip]
         L.wenc_attention_static.argtypes = [vp, vp, vp, vp, i, i, i, i, vp]
@@ -106,7 +107,7 @@ def lib() -> ctypes.CDLL:
                      "wenc_layernorm", "wenc_linear", "wenc_sync_status", "wenc_forward_launches",
                      "wenc_selftest_wait_timeout", "wenc_linear_tf32", "wenc_attention_tf32", "wenc_set_stem",
                      "wenc_stem", "wenc_encode", "wenc_encode_launches", "wenc_set_cross_kv", "wenc_cross_kv",
-                     "wenc_selftest_gemm_schedule"):
+                     "wenc_selftest_gemm_schedule", "wenc_selftest_gemm_pair_abort"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -371,6 +372,22 @@ def attention_tf32(q, k, v, out=None, stream=None):
         out = torch.empty_like(q)
     _require(out, torch.float32, "out")
     _check(lib().wenc_attention_tf32(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, T, H, hd, _stream(stream)))
+    return out
+
+
+def selftest_gemm_pair_abort(a, w, bias, stop_after: int, out=None, stream=None):
+    """Launch the CTA-pair GEMM self-test (the odd CTA of each pair stops after `stop_after`
+    k-blocks); returns the (undefined) output tensor; read the outcome with sync_status()."""
+    import torch
+    _require(a, torch.bfloat16, "a")
+    _require(w, torch.bfloat16, "w")
+    _require(bias, torch.float32, "bias")
+    M, K = a.shape
+    N = w.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    _check(lib().wenc_selftest_gemm_pair_abort(_ptr(a), _ptr(w), _ptr(bias), _ptr(out), M, N, K, int(stop_after),
+                                              _stream(stream)))
     return out
 
 
