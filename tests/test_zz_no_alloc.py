@@ -95,3 +95,9 @@ def test_static_scratch_attention_refuses_oversized_problems():
                                  H, 64, vp(torch.cuda.current_stream().cuda_stream))
     assert st == 1
     assert b"static buffer" in L.wenc_last_error()
+    # a following call that succeeds clears that message
+    (q, k, v), _ = _case(1, 300, 2, 5)
+    small = torch.empty_like(q)
+    assert _static_call(L, q, k, v, small, 1, 300, 2) == 0
+    torch.cuda.synchronize()
+    assert L.wenc_last_error() == b""

@@ -56,6 +56,7 @@ using namespace wenc_host;
 
 // Defined in api.cu: status helpers and the handle-less device error word.
 wenc_status wenc_internal_fail(wenc_status s, const char* msg);
+void wenc_internal_clear_error();
 uint32_t* wenc_internal_error_word(std::string* why);
 bool wenc_internal_is_sm103(std::string* why);
 int wenc_internal_sm_count();
@@ -65,6 +66,7 @@ extern "C" WENC_API size_t wenc_attention_static_capacity(void) { return kStatic
 extern "C" WENC_API wenc_status wenc_attention_static(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                                       uint16_t* out, int B, int T, int H, int hd,
                                                       wenc_stream_t stream) {
+  wenc_internal_clear_error();  // a successful call leaves no message from an earlier failure
   if (!q || !k || !v || !out) return wenc_internal_fail(WENC_ERR_INVALID_ARG, "q/k/v/out is NULL");
   if (B < 1 || T < 1 || H < 1) return wenc_internal_fail(WENC_ERR_INVALID_ARG, "B, T, H must be >= 1");
   if (hd != 64) return wenc_internal_fail(WENC_ERR_UNSUPPORTED, "head_dim must be 64");
