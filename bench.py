@@ -7,9 +7,14 @@
 A step is one wenc_forward call over one batch of synthetic windows (all blocks + the final
 LayerNorm). Default workload: the large-dims stack (32 blocks, batch 16, T 1500, d 1280,
 20 heads x 64, ffn 5120). Weights and inputs are seeded synthetic tensors (no checkpoint).
-`value` is windows/s with the input already in HBM; `e2e` is the same metric through the
-same C-ABI call with the input copied from pinned host memory and the output copied back
-inside the timed region. Multi-GPU runs are independent replicas (windows are independent;
+`value` is windows/s with the input already in HBM, timed over K steps with nothing armed but
+the library's launches; the per-kernel times (`kernels`, `roofline`) come from a second pass of
+the same K steps with the library's per-launch CUDA events armed. `e2e` is the same metric
+through the same C-ABI call with the input copied from pinned host memory and the output copied
+back inside the timed region. After the headline (one GPU, default workload) the line also
+carries `attention_sweep` (wenc_attention alone at B 16, H 20, T 256 / 1500 / 3000) and
+`configs` (the tiny block and the tiny, base and small stacks), each from CUDA events with the
+L2 flushed between calls; `--no-extras` skips both. Multi-GPU runs are independent replicas (windows are independent;
 there is no collective on the data path): value = all ranks' windows / the slowest rank's time.
 
 `--stem` makes a step the whole encoder from log-mel frames (wenc_encode: the convolutional stem,
@@ -248,7 +253,44 @@ def host_cores():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(w, seconds: float, with_stem: bool = False, with_cross: bool = False):
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the platform's machine name)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+_ONE_THREAD_ENV = {"OPENBLAS_NUM_THREADS": "1", "OMP_NUM_THREADS": "1", "MKL_NUM_THREADS": "1",
+                   "BLIS_NUM_THREADS": "1", "VECLIB_MAXIMUM_THREADS": "1", "NUMEXPR_NUM_THREADS": "1"}
+
+
+def time_oracle_block_single_thread(w, runs: int = 2, timeout: float = 120.0):
+    """Seconds per block of the f64 oracle with one BLAS thread (a child process, since the BLAS
+    thread count is fixed when numpy loads); None if the child fails or runs out of time."""
+    code = ("import json, sys; sys.path.insert(0, %r); import bench, synth; "
+            "print(json.dumps(bench.time_oracle_block(synth.WORKLOADS[%r], 0.0, steps=%d)))" % (ROOT, w.name, runs))
+    env = dict(os.environ, **_ONE_THREAD_ENV)
+    try:
+        r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=timeout)
+        return statistics.median(json.loads(r.stdout.strip().splitlines()[-1])) if r.returncode == 0 else None
+    except Exception:
+        return None
+
+
+def cpu_baseline(w, seconds: float, with_stem: bool = False, with_cross: bool = False, single_thread: bool = True):
     times = time_oracle_block(w, seconds)
     t_block = statistics.median(times)
     t_stem = statistics.median(time_oracle_stem(w, 3)) if with_stem else 0.0
@@ -257,11 +299,20 @@ def cpu_baseline(w, seconds: float, with_stem: bool = False, with_cross: bool = 
     stem_note = f" + the stem ({t_stem:.3f} s, median of 3)" if with_stem else ""
     if with_cross:
         stem_note += f" + cross K/V of 2 decoder layers x{w.n_layers / 2:g} ({t_cross:.3f} s)"
-    return {"value": win_s, "unit": "windows/s", "cores": host_cores(), "kind": "oracle",
+    line = {"value": win_s, "unit": "windows/s", "cores": host_cores(), "kind": "oracle",
             "sample": (f"f64 numpy oracle, one block of one {w.seq_len}-frame window at {w.name} dims, "
                        f"median of {len(times)} runs ({t_block:.3f} s/block), extrapolated x{w.n_layers} blocks"
-                       + stem_note),
-            "seconds_per_block": t_block}
+                       + stem_note + "; all cores (BLAS threads = host cores)"),
+            "seconds_per_block": t_block, "cpu_model": cpu_model(), "nproc": os.cpu_count()}
+    if single_thread:
+        t1 = time_oracle_block_single_thread(w)
+        line["single_thread"] = (None if t1 is None else
+                                 {"value": 1.0 / (t1 * w.n_layers + t_stem + t_cross), "unit": "windows/s",
+                                  "cores": 1, "seconds_per_block": t1,
+                                  "sample": "the same block with one BLAS thread (median of 2 runs), extrapolated "
+                                            f"x{w.n_layers} blocks" + (" (stem and cross K/V at all cores)"
+                                                                       if with_stem or with_cross else "")})
+    return line
 
 
 # ------------------------------------------------------------------------------------------ arms
@@ -300,12 +351,116 @@ def run_reference(args, w):
     return 0
 
 
+def build_encoder(w, precision: str = "bf16"):
+    """The library's encoder over workload w's seeded synthetic weights; returns (encoder, the
+    generator positioned after the weights, from which the input is drawn)."""
+    import torch
+
+    import synth
+    from transformer_encoder_gb300 import Encoder
+    dev_layers = []
+
+    def up(p):
+        out = {}
+        for k, v in p.items():
+            t = torch.from_numpy(v)
+            if k in synth.MATRIX_KEYS and w.bf16_weights:
+                t = t.to(torch.bfloat16)
+            out[k] = t.cuda()
+        return out
+
+    _, final, rng = synth.make_weights(w, layer_callback=lambda p: dev_layers.append(up(p)))
+    fin = (torch.from_numpy(final[0]).cuda(), torch.from_numpy(final[1]).cuda()) if w.final_ln else None
+    enc = Encoder(dev_layers, w.n_heads, w.seq_len, w.batch, final=fin, precision=precision)
+    del dev_layers
+    torch.cuda.empty_cache()
+    return enc, rng
+
+
+def _l2_flush_buffer():
+    import torch
+    return torch.empty(64 << 20, dtype=torch.float32, device="cuda")  # 256 MB, twice the L2
+
+
+def attention_sweep(peaks, reps: int = 10):
+    """wenc_attention alone at B = 16, H = 20, hd = 64 for T in {256, 1500, 3000}: median CUDA-event
+    time per call (L2 flushed before each), TFLOP/s and fraction of the measured bf16 burst peak."""
+    import torch
+
+    from transformer_encoder_gb300 import attention, sync_status
+    B, H = 16, 20
+    flush = _l2_flush_buffer()
+    gen = torch.Generator(device="cuda").manual_seed(1)
+    res = {}
+    for T in (256, 1500, 3000):
+        q, k, v = (torch.randn(B, T, H, 64, device="cuda", generator=gen).to(torch.bfloat16) for _ in range(3))
+        out = torch.empty_like(q)
+        for _ in range(3):
+            attention(q, k, v, out)
+        evs = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            attention(q, k, v, out)
+            e1.record()
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        sync_status()
+        us = 1e3 * statistics.median(a.elapsed_time(b) for a, b in evs)
+        tf = 4.0 * B * H * T * T * 64 / (us * 1e-6) / 1e12
+        res[str(T)] = {"B": B, "H": H, "hd": 64, "us": us, "tflops": tf, "frac_of_bf16_burst": tf / peaks["bf16_tflops"],
+                       "launches": 1, "inputs": "q, k, v ~ N(0, 1) bf16 [B, T, H, 64], seed 1; L2 flushed before each call"}
+        del q, k, v, out
+    return res
+
+
+def configs_throughput(peaks, steps: int = 20, warmup: int = 3):
+    """The four smaller workloads (tiny block, tiny, base and small stacks): windows/s and TFLOP/s of
+    wenc_forward from CUDA events around each step, with the L2 flushed between steps (their
+    weights and activations would otherwise stay in the 126 MB L2)."""
+    import torch
+
+    import synth
+    res = {}
+    flush = _l2_flush_buffer()
+    for name in ("tiny_block", "tiny_stack", "base_stack", "small_stack"):
+        w = synth.WORKLOADS[name]
+        enc, rng = build_encoder(w)
+        x = torch.from_numpy(synth.make_input(w, rng)).cuda()
+        out = torch.empty_like(x)
+        for _ in range(warmup):
+            enc.forward(x, out)
+        evs = []
+        for _ in range(steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            enc.forward(x, out)
+            e1.record()
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        enc.sync_status()
+        ms = sum(a.elapsed_time(b) for a, b in evs)
+        tf = w.flops() * steps / (ms / 1e3) / 1e12
+        res[name] = {"workload": workload_desc(w), "windows_per_s": w.batch * steps / (ms / 1e3),
+                     "ms_per_step": ms / steps, "tflops": tf, "frac_of_bf16_burst": tf / peaks["bf16_tflops"],
+                     "launches_per_step": enc.launches(),
+                     "bound": ("latency: a forward this small is a few dozen microseconds of dependent launches"
+                               if w.flops() < 0.1e12 else "tensor (GEMMs) with latency at the launch boundaries"),
+                     "weights": "f32 (rounded to bf16 at create)" if not w.bf16_weights else "bf16"}
+        enc.close()
+        del x, out
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_wenc(args, w):
     import numpy as np
     import torch
 
     import synth
-    from transformer_encoder_gb300 import LAUNCH_KINDS, Encoder
+    from transformer_encoder_gb300 import LAUNCH_KINDS
 
     rank, local_rank, world = dist_env()
     if not torch.cuda.is_available():
@@ -323,23 +478,8 @@ def run_wenc(args, w):
     peaks, peak_src = load_peaks()
 
     # ---- weights and inputs (seeded synthetic; identical on every rank)
-    dev_layers = []
-
-    def up(p):
-        out = {}
-        for k, v in p.items():
-            t = torch.from_numpy(v)
-            if k in synth.MATRIX_KEYS and w.bf16_weights:
-                t = t.to(torch.bfloat16)
-            out[k] = t.cuda()
-        return out
-
-    _, final, rng = synth.make_weights(w, layer_callback=lambda p: dev_layers.append(up(p)))
-    fin = (torch.from_numpy(final[0]).cuda(), torch.from_numpy(final[1]).cuda()) if w.final_ln else None
-    enc = Encoder(dev_layers, w.n_heads, w.seq_len, w.batch, final=fin, precision=args.precision)
+    enc, rng = build_encoder(w, args.precision)
     tf32 = args.precision == "tf32"
-    del dev_layers
-    torch.cuda.empty_cache()
     if args.stem:
         stem = synth.make_stem(w)
         enc.set_stem({k: (torch.from_numpy(v).to(torch.bfloat16) if k in ("conv1_w", "conv2_w") and w.bf16_weights
@@ -374,13 +514,7 @@ def run_wenc(args, w):
     torch.cuda.synchronize()
     enc.sync_status()
 
-    # ---- timed region: K steps, per-launch events armed on every step
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_launch + 1)] for _ in range(args.steps)]
-    for row in ev:  # torch creates the CUDA event on its first record; the library needs real handles
-        for e in row:
-            e.record(stream)
-    torch.cuda.synchronize()
-    kinds = None
+    # ---- timed region (the headline): K steps with nothing armed but the library's own launches
     clocks = ClockSampler(local_rank)
     clocks.start()
     time.sleep(0.3)
@@ -389,6 +523,25 @@ def run_wenc(args, w):
     t_start = torch.cuda.Event(enable_timing=True)
     t_stop = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
+    for _ in range(args.steps):
+        step(x, out)
+    t_stop.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ms_total = t_start.elapsed_time(t_stop)
+    enc.sync_status()
+
+    # ---- per-kernel breakdown: a second pass of K steps with the library's per-launch events armed
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_launch + 1)] for _ in range(args.steps)]
+    for row in ev:  # torch creates the CUDA event on its first record; the library needs real handles
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
+    kinds = None
+    k_start = torch.cuda.Event(enable_timing=True)
+    k_stop = torch.cuda.Event(enable_timing=True)
+    k_start.record(stream)
     for k in range(args.steps):
         if args.cross_kv:
             # the timing hook covers one library call: arm it for the encoder, then for the
@@ -403,11 +556,9 @@ def run_wenc(args, w):
             step(x, out)
         if kinds is None:
             kinds = ks
-    t_stop.record(stream)
+    k_stop.record(stream)
     torch.cuda.synchronize()
-    barrier()
-    clk = clocks.stop()
-    ms_total = t_start.elapsed_time(t_stop)
+    ms_hooked = k_start.elapsed_time(k_stop)
     enc.sync_status()
 
     # per-kind device time over the timed region
@@ -554,17 +705,28 @@ def run_wenc(args, w):
                              "source": peak_src},
         "roofline": roofline,
         "kernels": kern,
+        "kernels_pass": {"ms_per_step": ms_hooked / args.steps,
+                         "note": "the per-kernel times come from a second pass of the same K steps with the "
+                                 "library's per-launch CUDA events armed; value and ms_per_step come from a pass "
+                                 "without them"},
         "gpu_launches": n_launch * args.steps,
         "e2e": {"value": windows * args.steps / (ms_e2e / 1e3), "unit": "windows/s",
                 "h2d_bytes_per_step": x.numel() * 4, "d2h_bytes_per_step": out.numel() * 4,
                 "copies": "pinned host memory, on a copy stream overlapping the previous/next step (double-buffered)"},
         "clocks": clk,
     }
+    enc.close()
+    del x, out, xs, outs
+    torch.cuda.empty_cache()
+    extras = (world == 1 and not args.no_extras and w.name == "large_stack" and not tf32
+              and not args.stem and not args.cross_kv)
+    if extras:
+        line["attention_sweep"] = attention_sweep(peaks)
+        line["configs"] = configs_throughput(peaks)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, with_stem=args.stem, with_cross=args.cross_kv)
     if rank == 0:
         print(json.dumps(line), flush=True)
-    enc.close()
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -580,6 +742,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="large_stack")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle's CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the standalone attention sweep and the four smaller workloads after the headline")
     ap.add_argument("--cross-kv", action="store_true",
                     help="add the decoder cross-attention K/V precompute over the encoder output to each step")
     ap.add_argument("--stem", action="store_true",
