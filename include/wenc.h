@@ -57,7 +57,7 @@ typedef enum {
   WENC_OK = 0,
   WENC_ERR_INVALID_ARG = 1,     /* null pointer, bad size, misaligned buffer */
   WENC_ERR_UNSUPPORTED = 2,     /* a shape or mode this build does not implement (e.g. hd != 64) */
-  WENC_ERR_OOM = 3,             /* device allocation failed (wenc_create only) */
+  WENC_ERR_OOM = 3,             /* device allocation failed (wenc_create, wenc_set_stem, wenc_set_cross_kv) */
   WENC_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed; see wenc_last_error() */
   WENC_ERR_DEVICE_TIMEOUT = 5   /* a bounded device-side wait ran out (pipeline stalled) */
 } wenc_status;
@@ -138,8 +138,10 @@ typedef struct wenc wenc; /* opaque handle */
  * engine does at open). `layers` holds cfg->n_layers entries; lnf_w/lnf_b [d] are read
  * only when cfg->final_ln is set (may be NULL otherwise). The caller's buffers may be
  * freed once this returns: it synchronises `stream` before returning.
- * Errors: INVALID_ARG (null/inconsistent sizes, bk != NULL), UNSUPPORTED (hd != 64,
- * d or f not a multiple of 128, seq_len > 4096), OOM, CUDA. On error *out is NULL. */
+ * Errors: INVALID_ARG (null/inconsistent sizes, bk != NULL, `stream` being captured into a
+ * CUDA graph: refused before it is touched, so the capture stays intact), UNSUPPORTED (hd != 64,
+ * d or f not a multiple of 128, seq_len > 4096), OOM (nothing stays allocated), CUDA. On error
+ * *out is NULL. */
 WENC_API wenc_status wenc_create(const wenc_config* cfg, const wenc_layer_weights* layers,
                         const float* lnf_w, const float* lnf_b, wenc_stream_t stream,
                         wenc** out);
@@ -167,7 +169,8 @@ WENC_API wenc_status wenc_forward_layers(wenc* h, const float* hidden_in, float*
  * over the unfolded signal, weights reordered to [C_out, 3*C_in]) and allocates the stem's
  * workspace for cfg.max_batch windows. A second call replaces the first. Synchronises `stream`
  * before returning; the caller's buffers may then be freed.
- * Errors: INVALID_ARG (NULL pointers, n_mels not a multiple of 8 or outside 8..1024), OOM, CUDA. */
+ * Errors: INVALID_ARG (NULL pointers, n_mels not a multiple of 8 or outside 8..1024, `stream`
+ * being captured), OOM (the handle keeps working without a stem; an earlier stem is gone), CUDA. */
 WENC_API wenc_status wenc_set_stem(wenc* h, const wenc_stem_weights* w, wenc_stream_t stream);
 
 /* wenc_stem -- hidden_out = stem(mel): mel float32 [B, 2*seq_len, n_mels] (time-major log-mel
@@ -188,7 +191,8 @@ WENC_API int wenc_encode_launches(const wenc* h);
  * pointers owned by the caller). They are packed into one [2 n_dec d, d] matrix in the handle's
  * precision (K of layer l at rows 2l*d.., V at (2l+1)*d..; K has no bias, as in
  * turbospark-runtime build_cross_caches). A second call replaces the first. Synchronises
- * `stream` before returning. Errors: INVALID_ARG (NULL pointers, n_dec_layers < 1), OOM, CUDA. */
+ * `stream` before returning. Errors: INVALID_ARG (NULL pointers, n_dec_layers < 1, `stream` being
+ * captured), OOM (the handle keeps working without cross K/V weights; earlier ones are gone), CUDA. */
 WENC_API wenc_status wenc_set_cross_kv(wenc* h, int n_dec_layers, const void* const* wk, const void* const* wv,
                                        const float* const* bv, wenc_stream_t stream);
 
@@ -285,6 +289,18 @@ WENC_API wenc_status wenc_linear_tf32(const float* A, const float* W, const floa
  * wenc_attention. */
 WENC_API wenc_status wenc_attention_tf32(const float* q, const float* k, const float* v, float* out,
                                          int B, int T, int H, int hd, wenc_stream_t stream);
+
+/* wenc_set_device_alloc_limit -- test hook for the out-of-memory path (the pages have no
+ * counterpart). Caps the device memory the library holds in its handles' arenas (weights,
+ * workspace, stem, cross K/V) at `bytes`; an allocation that would exceed the cap fails as if
+ * cudaMalloc had run out, so wenc_create, wenc_set_stem and wenc_set_cross_kv return
+ * WENC_ERR_OOM and release what they allocated. 0 removes the cap (the default). Process-wide;
+ * not meant for concurrent use with other threads creating handles. */
+WENC_API void wenc_set_device_alloc_limit(size_t bytes);
+
+/* wenc_device_bytes_held -- bytes of device memory the library holds in live arenas (all
+ * handles of the process), for leak checks. */
+WENC_API size_t wenc_device_bytes_held(void);
 
 /* wenc_selftest_wait_timeout -- exercises the failure path of the bounded device waits
  * (the pages have no counterpart). Launches one CTA

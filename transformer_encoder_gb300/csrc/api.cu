@@ -223,6 +223,7 @@ struct wenc {
   float2* part_ml = nullptr;      // split-key (max, sum) pairs (workspace)
   void* weight_arena = nullptr;
   void* work_arena = nullptr;
+  size_t weight_bytes = 0, work_bytes = 0, stem_bytes = 0, cross_bytes = 0;  // sizes of the four arenas
   uint32_t* err_host = nullptr;  // mapped pinned word: the device writes, the host reads without a sync
   uint32_t* err_dev = nullptr;
   // timing hook (one call)
@@ -245,6 +246,37 @@ struct wenc {
 };
 
 namespace {
+
+// Device memory the library holds (its handles' arenas), and an optional cap on it that a test
+// sets to make an allocation fail as if the device had run out (wenc_set_device_alloc_limit).
+std::atomic<size_t> g_dev_held{0};
+std::atomic<size_t> g_dev_limit{0};  // 0: no cap
+
+cudaError_t dev_alloc(void** p, size_t bytes) {
+  *p = nullptr;
+  const size_t cap = g_dev_limit.load();
+  if (cap != 0 && g_dev_held.load() + bytes > cap) return cudaErrorMemoryAllocation;
+  cudaError_t e = cudaMalloc(p, bytes);
+  if (e != cudaSuccess) {
+    *p = nullptr;
+    return e;
+  }
+  g_dev_held += bytes;
+  return cudaSuccess;
+}
+
+void dev_free(void*& p, size_t& bytes) {
+  if (!p) return;
+  cudaFree(p);
+  g_dev_held -= bytes;
+  p = nullptr;
+  bytes = 0;
+}
+
+// Entry points that synchronise their stream (create, set_stem, set_cross_kv) cannot run while
+// it is being captured into a CUDA graph: refuse such a stream before touching it, which keeps
+// the caller's capture intact.
+wenc_status check_sync_stream(wenc_stream_t stream, const char* what);
 
 struct Arena {
   size_t used = 0;
@@ -279,12 +311,25 @@ wenc_status check_config(const wenc_config* c) {
 
 void free_handle(wenc* h) {
   if (!h) return;
-  if (h->weight_arena) cudaFree(h->weight_arena);
-  if (h->work_arena) cudaFree(h->work_arena);
-  if (h->stem_arena) cudaFree(h->stem_arena);
-  if (h->cross_arena) cudaFree(h->cross_arena);
+  dev_free(h->weight_arena, h->weight_bytes);
+  dev_free(h->work_arena, h->work_bytes);
+  dev_free(h->stem_arena, h->stem_bytes);
+  dev_free(h->cross_arena, h->cross_bytes);
   if (h->err_host) cudaFreeHost(h->err_host);
   delete h;
+}
+
+wenc_status check_sync_stream(wenc_stream_t stream, const char* what) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(reinterpret_cast<cudaStream_t>(stream), &cs);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(WENC_ERR_INVALID_ARG, "%s: the stream is not usable (%s)", what, cudaGetErrorString(e));
+  }
+  if (cs != cudaStreamCaptureStatusNone)
+    return fail(WENC_ERR_INVALID_ARG, "%s synchronises its stream and cannot run while the stream is being captured",
+                what);
+  return WENC_OK;
 }
 
 // One matrix into the packed arena. BF16 precision: copied (bf16 source) or rounded to bf16
@@ -439,6 +484,10 @@ extern "C" {
 
 const char* wenc_last_error(void) { return g_last_error.c_str(); }
 
+void wenc_set_device_alloc_limit(size_t bytes) { g_dev_limit.store(bytes); }
+
+size_t wenc_device_bytes_held(void) { return g_dev_held.load(); }
+
 const char* wenc_version(void) { return "wenc 0.1 sm_103a"; }
 
 wenc_status wenc_create(const wenc_config* cfg, const wenc_layer_weights* layers, const float* lnf_w,
@@ -451,6 +500,8 @@ wenc_status wenc_create(const wenc_config* cfg, const wenc_layer_weights* layers
   if (!layers) return fail(WENC_ERR_INVALID_ARG, "layers is NULL");
   std::string why;
   if (!device_is_sm103(&why)) return fail(WENC_ERR_UNSUPPORTED, "%s", why.c_str());
+  st = check_sync_stream(stream_, "wenc_create");
+  if (st != WENC_OK) return st;
   const int L = cfg->n_layers, d = cfg->d_model, f = cfg->ffn_dim;
   for (int l = 0; l < L; ++l) {
     const wenc_layer_weights& w = layers[l];
@@ -496,7 +547,8 @@ wenc_status wenc_create(const wenc_config* cfg, const wenc_layer_weights* layers
     if (!h->tf32) o.cs_qkv = wa.take(3 * d * 4);
   }
   const size_t off_lnf_w = wa.take(d * 4), off_lnf_b = wa.take(d * 4);
-  cudaError_t e = cudaMalloc(&h->weight_arena, wa.used);
+  cudaError_t e = dev_alloc(&h->weight_arena, wa.used);
+  if (e == cudaSuccess) h->weight_bytes = wa.used;
   if (e != cudaSuccess) {
     cudaGetLastError();
     free_handle(h);
@@ -520,7 +572,8 @@ wenc_status wenc_create(const wenc_config* cfg, const wenc_layer_weights* layers
   const size_t part_rows = static_cast<size_t>(h->attn_splits) * cfg->max_batch * cfg->n_heads * cfg->seq_len;
   const size_t off_po = h->attn_splits > 1 ? ka.take(part_rows * wenc_host::kAttnHD * sizeof(float)) : 0;
   const size_t off_pml = h->attn_splits > 1 ? ka.take(part_rows * sizeof(float2)) : 0;
-  e = cudaMalloc(&h->work_arena, ka.used);
+  e = dev_alloc(&h->work_arena, ka.used);
+  if (e == cudaSuccess) h->work_bytes = ka.used;
   if (e != cudaSuccess) {
     cudaGetLastError();
     free_handle(h);
@@ -710,6 +763,8 @@ wenc_status wenc_set_stem(wenc* h, const wenc_stem_weights* w, wenc_stream_t str
   }
   if (w->n_mels < 8 || w->n_mels > 1024 || w->n_mels % 8 != 0)
     return fail(WENC_ERR_INVALID_ARG, "n_mels %d: a multiple of 8 in 8..1024", w->n_mels);
+  const wenc_status sst = check_sync_stream(stream_, "wenc_set_stem");
+  if (sst != WENC_OK) return sst;
   const wenc_config& c = h->cfg;
   const int d = c.d_model, T = c.seq_len, nm = w->n_mels;
   const size_t es = h->esz;
@@ -721,16 +776,15 @@ wenc_status wenc_set_stem(wenc* h, const wenc_stem_weights* w, wenc_stream_t str
   const size_t o_a1 = ar.take(rows1 * kp1 * es), o_h1 = ar.take(rows1 * d * es), o_a2 = ar.take(rows2 * 3 * d * es);
   if (h->stem_arena) {
     cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream_));
-    cudaFree(h->stem_arena);
-    h->stem_arena = nullptr;
+    dev_free(h->stem_arena, h->stem_bytes);
   }
   h->has_stem = false;
-  cudaError_t e = cudaMalloc(&h->stem_arena, ar.used);
+  cudaError_t e = dev_alloc(&h->stem_arena, ar.used);
   if (e != cudaSuccess) {
     cudaGetLastError();
-    h->stem_arena = nullptr;
     return fail(WENC_ERR_OOM, "stem: cudaMalloc(%zu) failed", ar.used);
   }
+  h->stem_bytes = ar.used;
   uint8_t* base = static_cast<uint8_t*>(h->stem_arena);
   h->n_mels = nm;
   h->kp1 = kp1;
@@ -813,24 +867,25 @@ wenc_status wenc_set_cross_kv(wenc* h, int n_dec, const void* const* wk, const v
       if (!is_device_accessible(p)) return fail(WENC_ERR_INVALID_ARG, "decoder layer %d: not device memory", l);
     }
   }
+  const wenc_status sst = check_sync_stream(stream_, "wenc_set_cross_kv");
+  if (sst != WENC_OK) return sst;
   const wenc_config& c = h->cfg;
   const int d = c.d_model;
   const size_t es = h->esz, n_out = size_t(2) * n_dec * d;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream_);
   if (h->cross_arena) {
     cudaStreamSynchronize(s);
-    cudaFree(h->cross_arena);
-    h->cross_arena = nullptr;
+    dev_free(h->cross_arena, h->cross_bytes);
   }
   h->n_dec = 0;
   Arena ar;
   const size_t o_w = ar.take(n_out * d * es), o_b = ar.take(n_out * 4);
-  cudaError_t e = cudaMalloc(&h->cross_arena, ar.used);
+  cudaError_t e = dev_alloc(&h->cross_arena, ar.used);
   if (e != cudaSuccess) {
     cudaGetLastError();
-    h->cross_arena = nullptr;
     return fail(WENC_ERR_OOM, "cross K/V: cudaMalloc(%zu) failed", ar.used);
   }
+  h->cross_bytes = ar.used;
   uint8_t* base = static_cast<uint8_t*>(h->cross_arena);
   h->wx = base + o_w;
   h->bx = reinterpret_cast<float*>(base + o_b);
@@ -1063,6 +1118,8 @@ wenc_status wenc_sync_status(wenc* h) {
     }
     if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
   }
+  if (word != 0 && (word & 0xffu) == WENC_ERR_CUDA)
+    return fail(WENC_ERR_CUDA, "an index check of the bounds-checked build failed (site %u)", (word >> 8) & 0xffu);
   if (word != 0)
     return fail(WENC_ERR_DEVICE_TIMEOUT, "device wait ran out (code %u, site %u)", word & 0xffu, (word >> 8) & 0xffu);
   return WENC_OK;

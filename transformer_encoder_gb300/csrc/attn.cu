@@ -121,6 +121,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // window (all of them when n_splits == 1).
   const int n_kv_all = (T + BKV - 1) / BKV;
   const int n_x = ((T + 2 * BQ - 1) / (2 * BQ)) * n_splits;
+  const int n_windows = n_items / (n_x * H);
   struct Item {
     int q0, h, b, split, kv0, n_kv;
   };
@@ -207,6 +208,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int w = blockIdx.x, i = 0; ok && w < n_items; w += gridDim.x, ++i) {
         const Item it = decode(w);
         const int qb = i & 1;
+        if (!in_bounds(it.q0 >= 0 && it.q0 < T && it.h >= 0 && it.h < H && it.b >= 0 && it.b < n_windows &&
+                           it.kv0 >= 0 && it.n_kv >= 1 && it.kv0 + it.n_kv <= n_kv_all && it.split < n_splits,
+                       err, 72)) {
+          *abort_flag = 1u;  // an item outside the problem: stop as a failed wait would
+          break;
+        }
         if (!mbar_wait(q_empty(qb), ((i >> 1) & 1) ^ 1u, wc, 9)) break;
         mbar_arrive_expect_tx(q_full(qb), 2 * Q_BYTES);
         tma_load_3d(sQ + qb * 2 * Q_BYTES, &tq, q_full(qb), q_col0 + it.h * HD, it.q0, it.b);
@@ -414,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t o[32];
             tmem_ld_32x32b_x32(tO(t) + lane_off + half * 32, o);
             tmem_ld_wait();
-            if (tq_row < T) {
+            if (tq_row < T && in_bounds(it.b < n_windows && it.h * HD + HD <= out_stride, err, 73)) {
               uint4* d4 = reinterpret_cast<uint4*>(dst + half * 32);
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
@@ -433,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t o[32];
             tmem_ld_32x32b_x32(tO(t) + lane_off + half * 32, o);
             tmem_ld_wait();
-            if (tq_row < T) {
+            if (tq_row < T && in_bounds(pi < static_cast<size_t>(n_splits) * n_windows * H * T, err, 74)) {
               float4* d4 = reinterpret_cast<float4*>(part_o + pi * HD + half * 32);
 #pragma unroll
               for (int q = 0; q < 8; ++q)

@@ -226,7 +226,8 @@ template <int EPI, bool F32OUT>
 __device__ __forceinline__ void epilogue_chunk(const uint32_t (&acc)[32], uint32_t stage, int lane, int grow0, int M,
                                                int N, int col, const float* __restrict__ bias,
                                                const float4 (&rr)[8], void* out, int plane,
-                                               const wenc_host::GemmExtra& ex, RowState& rs, int chunk) {
+                                               const wenc_host::GemmExtra& ex, RowState& rs, int chunk,
+                                               uint32_t* err) {
 #pragma unroll
   for (int q = 0; q < 8; ++q)
     st_shared_v4(stage_addr(stage, lane, q), acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
@@ -254,7 +255,7 @@ __device__ __forceinline__ void epilogue_chunk(const uint32_t (&acc)[32], uint32
       chunk_stats32(v, cm, cq);
       chunk_merge32(rs.a[i], rs.b[i], cm, cq, chunk);
     }
-    if (grow < M) {
+    if (grow < M && in_bounds(grow >= 0 && col >= 0 && col + 4 * cl + 4 <= N, err, 66)) {
       size_t off = static_cast<size_t>(grow) * N + col + 4 * cl;
       if constexpr (EPI == 4) {  // the chunk's 32 columns lie in one plane (plane % 32 == 0)
         const int pl = col / plane;
@@ -460,6 +461,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                      (PAIR ? static_cast<int>(rank) * (half < 0 ? BN / 2 : BN / 4) : 0);
       const bool hb = half >= 0 && half_box;
       const uint32_t stage_bytes = hb ? C::A_BYTES + C::B_BYTES / 2 : C::STAGE_BYTES;
+      if (!in_bounds(tile >= 0 && tile < num_tiles && n0 >= 0 && n0 < N && m0 >= 0, err, 64)) {
+        *abort_flag = 1u;  // the tile schedule left the output: stop as a failed wait would
+        ok = false;
+        break;
+      }
       for (int kb = 0; kb < k_blocks; ++kb) {
         if (PAIR && rank != 0 && ex.stop_odd_after >= 0 && loads >= static_cast<uint32_t>(ex.stop_odd_after)) {
           // self-test: this producer gives up here as if a wait had run out (site 31)
@@ -658,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) release_acc(acc);
         }
         epilogue_chunk<EPI, TF32>(r, stage, lane, grow0, M, N, c0 + c * 32, bias, rb[c & 1], out, row_period, ex, rs,
-                                  c);
+                                  c, err);
         if constexpr (kRowInput) {
           if (c + 2 < CH) {
             load_resid(rb[c & 1], resid, grow0, M, N, c0 + (c + 2) * 32, lane, row_period);

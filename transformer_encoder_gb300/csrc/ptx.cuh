@@ -9,8 +9,23 @@
 
 namespace wenc_dev {
 
-// Device error word codes (low byte = wenc_status, next byte = the wait site).
+// Device error word codes (low byte = wenc_status, next byte = the wait or check site).
 constexpr uint32_t kErrTimeout = 5u;
+constexpr uint32_t kErrIndex = 4u;  // WENC_ERR_CUDA: an index check of the bounds-checked build failed
+
+// Index checks of the bounds-checked build (compiled with -DWENC_BOUNDS_CHECK): a checked access
+// runs only if in_bounds() returns true; when its condition fails, the kernel records
+// kErrIndex | site << 8 in the device error word and skips the access (no trap, no early return,
+// so every barrier, wait and TMEM release of the kernel still happens). In the normal build the
+// checks compile to nothing.
+#ifdef WENC_BOUNDS_CHECK
+__device__ __forceinline__ bool in_bounds(bool ok, uint32_t* err, uint32_t site) {
+  if (!ok) *reinterpret_cast<volatile uint32_t*>(err) = kErrIndex | (site << 8);
+  return ok;
+}
+#else
+__device__ __forceinline__ constexpr bool in_bounds(bool, uint32_t*, uint32_t) { return true; }
+#endif
 // A wait that has not completed after this long is treated as a stalled pipeline.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 

@@ -17,7 +17,9 @@ __all__ = [
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-lib_path = os.path.join(_PKG, "_lib", "libwenc.so")
+# WENC_LIBRARY may name another library built in-tree into _lib/ (the index-checked
+# libwenc_bounds.so); anything outside _lib/ is refused.
+lib_path = os.path.join(_PKG, "_lib", os.path.basename(os.environ.get("WENC_LIBRARY") or "libwenc.so"))
 
 EPI_BIAS_BF16, EPI_BIAS_GELU_BF16, EPI_BIAS_RESID_F32 = 0, 1, 2
 LN_OUT_F32, LN_OUT_BF16, LN_OUT_TF32 = 0, 1, 2
@@ -33,6 +35,7 @@ EXPORTED_SYMBOLS = (
     "wenc_version", "wenc_selftest_wait_timeout", "wenc_attention_static", "wenc_attention_static_capacity",
     "wenc_linear_tf32", "wenc_attention_tf32", "wenc_set_stem", "wenc_stem", "wenc_encode", "wenc_encode_launches",
     "wenc_set_cross_kv", "wenc_cross_kv", "wenc_selftest_gemm_schedule", "wenc_selftest_gemm_pair_abort",
+    "wenc_set_device_alloc_limit", "wenc_device_bytes_held",
 )
 
 
@@ -93,6 +96,10 @@ def lib() -> ctypes.CDLL:
         L.wenc_sync_status.argtypes = [vp]
         L.wenc_selftest_wait_timeout.argtypes = [vp]
         L.wenc_selftest_gemm_pair_abort.argtypes = [vp, vp, vp, vp, i, i, i, i, vp]
+        L.wenc_set_device_alloc_limit.argtypes = [ctypes.c_size_t]
+        L.wenc_set_device_alloc_limit.restype = None
+        L.wenc_device_bytes_held.argtypes = []
+        L.wenc_device_bytes_held.restype = ctypes.c_size_t
         ip = ctypes.POINTER(ctypes.c_int)
         L.wenc_selftest_gemm_schedule.argtypes = [i, i, i, i, ip, i, ip, ip, ip]
         L.wenc_attention_static.argtypes = [vp, vp, vp, vp, i, i, i, i, vp]
