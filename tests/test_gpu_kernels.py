@@ -45,10 +45,11 @@ def test_layernorm_matches_oracle(rows, d, out_bf16):
 
 # ----------------------------------------------------------------------------- GEMM + epilogues
 # N % 256 == 0 runs on CTA pairs (256-row tiles): M = 1 and M = 100 leave the pair's second CTA
-# without a valid row, M = 129 with one.
+# without a valid row, M = 129 with one. M = 1500 and M = 24000 with N = 1280 run half-width
+# units (all of them, or the last partial wave of a 470-tile launch).
 @pytest.mark.parametrize("M,N,K", [(1537, 1152, 384), (300, 384, 1536), (1500, 2048, 512), (129, 256, 64),
                                    (3000, 1280, 1280), (6000, 1280, 512), (1537, 640, 256), (1, 256, 64),
-                                   (100, 768, 192)])
+                                   (100, 768, 192), (1500, 1280, 1280), (24000, 1280, 256)])
 @pytest.mark.parametrize("epi", [0, 1, 2])
 def test_linear_matches_oracle(M, N, K, epi):
     torch = _torch()
