@@ -106,6 +106,13 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
+// Arrivals with relaxed semantics: they order nothing but the arrival itself (see release_acc).
+__device__ __forceinline__ void mbar_arrive_relaxed_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_relaxed(uint32_t bar) {
+  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
 // Count `bytes` as arrived on this CTA's barrier without a copy (for a copy that was expected but
 // never issued).
 __device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
@@ -579,10 +586,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int col_half = (warp - 2) >> 2;
     const uint32_t stage = smem_u32(smem + STAGES * C::STAGE_BYTES) + (warp - 2) * C::EPI_STAGE_BYTES;
     auto row0_of = [&](int t) { return tile_m(t) * TM + static_cast<int>(rank) * BM + quad * 32; };
-    // the barrier that frees an accumulator lives in the issuing CTA (the pair's even one)
+    // The barrier that frees an accumulator lives in the issuing CTA (the pair's even one). The
+    // arrival is relaxed: all it orders is this warp's TMEM reads (complete at tcgen05.wait::ld,
+    // and fenced by tcgen05.fence::before_thread_sync) before the next MMA overwrites the
+    // accumulator; a release would also wait for the warp's earlier global stores of the tile to
+    // be performed, stalling the epilogue for nothing.
     auto release_acc = [&](int a) {
-      if constexpr (PAIR) mbar_arrive_cluster(map_to_rank(tempty_bar(a), 0));
-      else mbar_arrive(tempty_bar(a));
+      if constexpr (PAIR) mbar_arrive_relaxed_cluster(map_to_rank(tempty_bar(a), 0));
+      else mbar_arrive_relaxed(tempty_bar(a));
     };
     auto col_of = [&](int t) { return tile_n(t) * BN + col_half * (BN / 2); };
     float4 rb[2][8];
