@@ -520,16 +520,19 @@ def run_wenc(args, w):
     time.sleep(0.3)
     barrier()
     torch.cuda.synchronize()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_stop = torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    for _ in range(args.steps):
+    step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    step_ev[0].record(stream)
+    for k in range(args.steps):
         step(x, out)
-    t_stop.record(stream)
+        step_ev[k + 1].record(stream)
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
-    ms_total = t_start.elapsed_time(t_stop)
+    ms_total = step_ev[0].elapsed_time(step_ev[-1])
+    step_ms = sorted(step_ev[k].elapsed_time(step_ev[k + 1]) for k in range(args.steps))
+
+    def pct(q):
+        return step_ms[min(len(step_ms) - 1, int(round(q * (len(step_ms) - 1))))]
     enc.sync_status()
 
     # ---- per-kernel breakdown: a second pass of K steps with the library's per-launch events armed
@@ -691,6 +694,7 @@ def run_wenc(args, w):
         "metric": METRIC, "value": value, "unit": "windows/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "tf32" if tf32 else "bf16", "data": "synthetic",
+        "ms_per_step_pct": {"p10": pct(0.1), "p50": pct(0.5), "p90": pct(0.9), "from": "CUDA events between steps"},
         "config": {"workload": workload_desc(w) + (f", from {2 * T} log-mel frames x {w.n_mels} through the "
                                                    "convolutional stem" if args.stem else "")
                    + (f", plus the cross-attention K/V of {w.n_layers} decoder layers (e2e reads back the encoder "

@@ -324,6 +324,18 @@ WENC_API wenc_status wenc_selftest_gemm_pair_abort(const uint16_t* A, const uint
                                                    uint16_t* out, int M, int N, int K, int stop_after,
                                                    wenc_stream_t stream);
 
+/* wenc_selftest_attention_abort -- exercises the failure path of the attention kernel (the pages
+ * have no counterpart). Runs the attention of wenc_attention (same arguments and layouts; no key
+ * splits) with its TMA producer giving up after `stop_after` K tiles, as if one of its waits had
+ * run out. The MMA and softmax warps then see the CTA's abort flag and stop, the producer drains
+ * the copies it issued, every MMA completes before TMEM is freed, and WENC_ERR_DEVICE_TIMEOUT
+ * (site 31) is recorded in the handle-less device error word. There is no trap, the context
+ * stays usable, and `out` holds no defined values. Stream-ordered; read the outcome with
+ * wenc_sync_status(NULL). */
+WENC_API wenc_status wenc_selftest_attention_abort(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                                   uint16_t* out, int B, int T, int H, int stop_after,
+                                                   wenc_stream_t stream);
+
 /* wenc_selftest_gemm_schedule -- host only, no device work: replays how a contraction of
  * M x N output elements divides its tiles among the units of one launch (single CTAs on
  * 128-row tiles when pair is 0, CTA pairs on 256 x 256 tiles when pair is 1), through the same

@@ -41,6 +41,8 @@ def test_bench_line_keeps_the_contract():
     assert e["unit"] == "windows/s" and e["value"] > 0
     assert e["h2d_bytes_per_step"] == e["d2h_bytes_per_step"] == 1500 * 384 * 4
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(d["clocks"])
+    pc = d["ms_per_step_pct"]
+    assert pc["p10"] <= pc["p50"] <= pc["p90"] and abs(pc["p50"] - d["ms_per_step"]) < 0.5 * d["ms_per_step"]
     assert "attention_sweep" not in d and "configs" not in d  # only after the default workload's headline
 
 

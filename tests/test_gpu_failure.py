@@ -68,3 +68,31 @@ def test_cta_pair_gemm_abort_drains_and_context_survives(stop_after):
     got = bf16_to_f64(out)
     assert (np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 2e-5 * np.sqrt(np.mean(ref * ref))).all()
     sync_status()
+
+
+@pytest.mark.parametrize("stop_after", [0, 40])
+def test_attention_abort_drains_and_context_survives(stop_after):
+    """The attention's TMA producer gives up after `stop_after` K tiles in every CTA (B 16, H 20,
+    T 1500: ~156 tiles per CTA, so 40 stops it mid-way through its items). The MMA and softmax
+    warps see the abort and stop, the copies in flight drain and TMEM is freed: the status reads
+    DEVICE_TIMEOUT within seconds, and attention run normally next passes the oracle gate."""
+    import torch
+    from transformer_encoder_gb300 import WencError, attention, selftest_attention_abort, sync_status
+    sync_status()
+    g = torch.Generator(device="cuda").manual_seed(9)
+    q, k, v = (torch.randn(16, 1500, 20, 64, device="cuda", generator=g).to(torch.bfloat16) for _ in range(3))
+    t0 = time.time()
+    selftest_attention_abort(q, k, v, stop_after)
+    with pytest.raises(WencError, match="DEVICE_TIMEOUT") as ei:
+        sync_status()
+    assert time.time() - t0 < 30.0
+    assert "site 31" in str(ei.value)
+    sync_status()
+    del q, k, v
+    qs, ks, vs = synth.make_qkv(2, 700, 3, 64, seed=4)
+    to_t = lambda a: torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
+    out = attention(to_t(qs), to_t(ks), to_t(vs))
+    torch.cuda.synchronize()
+    f = lambda a: synth.bf16_bits_to_f32(a).reshape(2, 700, 192)
+    attention_gate(bf16_to_f64(out).reshape(2, 700, 192), f(qs), f(ks), f(vs), 3, what="after the attention abort")
+    sync_status()

@@ -104,7 +104,10 @@ def _attn_case(B, T, H, scale, seed):
     return (to_t(q), to_t(k), to_t(v)), (to_f(q), to_f(k), to_f(v))
 
 
-@pytest.mark.parametrize("B,T,H", [(2, 1500, 3), (1, 256, 2), (3, 200, 1), (1, 64, 2), (1, 130, 1), (2, 3000, 1)])
+# T = 127 and 129 sit one key either side of the 128-key tile; T = 255 and 257 of two tiles (a
+# query pair); B = 3 windows make the windows' rows interleave across work items.
+@pytest.mark.parametrize("B,T,H", [(2, 1500, 3), (1, 256, 2), (3, 200, 1), (1, 64, 2), (1, 130, 1), (2, 3000, 1),
+                                   (3, 127, 2), (1, 129, 2), (2, 255, 1), (1, 257, 3)])
 @pytest.mark.parametrize("scale", [1.0, 0.1])
 def test_attention_matches_oracle(B, T, H, scale):
     torch = _torch()

@@ -1088,6 +1088,31 @@ wenc_status wenc_selftest_gemm_pair_abort(const uint16_t* A, const uint16_t* W, 
   return WENC_OK;
 }
 
+wenc_status wenc_selftest_attention_abort(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* out, int B,
+                                          int T, int H, int stop_after, wenc_stream_t stream) {
+  g_last_error.clear();
+  if (!q || !k || !v || !out) return fail(WENC_ERR_INVALID_ARG, "q/k/v/out is NULL");
+  if (B < 1 || T < 1 || H < 1 || stop_after < 0) return fail(WENC_ERR_INVALID_ARG, "B, T, H >= 1 and stop_after >= 0");
+  if (T > (1 << 20)) return fail(WENC_ERR_UNSUPPORTED, "T %d too large", T);
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(WENC_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
+  std::string why;
+  if (!device_is_sm103(&why)) return fail(WENC_ERR_UNSUPPORTED, "%s", why.c_str());
+  uint32_t* err = global_error_word(&why);
+  if (!err) return fail(WENC_ERR_CUDA, "%s", why.c_str());
+  const uint64_t row = uint64_t(H) * 64;
+  CUtensorMap tq, tk, tv;
+  bool ok = wenc_host::make_tmap_3d_bf16(&tq, q, row, T, B, row * 2, row * 2 * T, 64, wenc_host::kAttnBQ, &why) &&
+            wenc_host::make_tmap_3d_bf16(&tk, k, row, T, B, row * 2, row * 2 * T, 64, wenc_host::kAttnBKV, &why) &&
+            wenc_host::make_tmap_3d_bf16(&tv, v, row, T, B, row * 2, row * 2 * T, 64, wenc_host::kAttnBKV, &why);
+  if (!ok) return fail(WENC_ERR_INVALID_ARG, "%s", why.c_str());
+  cudaError_t e = wenc_host::launch_attention_main(tq, tk, tv, 0, 0, 0, out, static_cast<int>(row), B, T, H, err,
+                                                   reinterpret_cast<cudaStream_t>(stream), 1, nullptr, nullptr,
+                                                   stop_after);
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  return WENC_OK;
+}
+
 wenc_status wenc_selftest_gemm_schedule(int M, int N, int pair, int max_units, int* cover, int cover_len,
                                         int* unit_halves, int* units, int* halves) {
   g_last_error.clear();

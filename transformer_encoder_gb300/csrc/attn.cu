@@ -90,7 +90,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tv, int q_col0, int k_col0, int v_col0,
                     uint16_t* __restrict__ out, int out_stride, int T, int H, int n_items, float scale_log2,
                     int n_splits, int tiles_per_split, float* __restrict__ part_o, float2* __restrict__ part_ml,
-                    uint32_t* err) {
+                    uint32_t* err, int stop_after) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s0 = smem_u32(smem);
@@ -189,6 +189,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // V[n-1]; the next item's Q and first K tiles load while this item's last tiles run.
       int kc = 0, vc = 0, qi = 0;  // K tiles, V tiles and items issued
       auto load_k = [&](const Item& it, int j) -> bool {
+        if (stop_after >= 0 && kc >= stop_after) {
+          // self-test: this producer gives up here as if a wait had run out (site 31)
+          *abort_flag = 1u;
+          *reinterpret_cast<volatile uint32_t*>(err) = kErrTimeout | (31u << 8);
+          return false;
+        }
         const int st = kc % NK;
         if (!mbar_wait(k_empty(st), ((kc / NK) & 1) ^ 1u, wc, 11)) return false;
         mbar_arrive_expect_tx(k_full(st), KV_BYTES);
@@ -529,7 +535,8 @@ static int clamp_splits(int T, int n_splits) {
 
 cudaError_t launch_attention_main(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, int q_col0,
                                   int k_col0, int v_col0, uint16_t* out, int out_stride, int B, int T, int H,
-                                  uint32_t* err, cudaStream_t stream, int n_splits, float* part_o, float2* part_ml) {
+                                  uint32_t* err, cudaStream_t stream, int n_splits, float* part_o, float2* part_ml,
+                                  int stop_after) {
   if (B <= 0 || T <= 0 || H <= 0) return cudaSuccess;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -562,7 +569,8 @@ cudaError_t launch_attention_main(const CUtensorMap& tq, const CUtensorMap& tk, 
   // w = blockIdx.x + k * gridDim.x.
   const int grid = static_cast<int>(items < num_sms ? items : num_sms);
   return launch_pdl(attn_fwd_kernel, dim3(grid), dim3(kThreads), SMEM, stream, tq, tk, tv, q_col0, k_col0, v_col0,
-                    out, out_stride, T, H, static_cast<int>(items), scale_log2, n_splits, tps, part_o, part_ml, err);
+                    out, out_stride, T, H, static_cast<int>(items), scale_log2, n_splits, tps, part_o, part_ml, err,
+                    stop_after);
 }
 
 cudaError_t launch_attention_combine(const float* part_o, const float2* part_ml, uint16_t* out, int out_stride, int B,

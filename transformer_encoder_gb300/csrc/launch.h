@@ -132,9 +132,12 @@ cudaError_t launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const
                              uint32_t* err, cudaStream_t stream, int n_splits = 1, float* part_o = nullptr,
                              float2* part_ml = nullptr);
 // The two launches of launch_attention, separately (for per-launch accounting).
+// stop_after >= 0 (self-test only, wenc_selftest_attention_abort): the TMA producer gives up after
+// that many K tiles as if one of its waits had run out; -1 everywhere else.
 cudaError_t launch_attention_main(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, int q_col0,
                                   int k_col0, int v_col0, uint16_t* out, int out_stride, int B, int T, int H,
-                                  uint32_t* err, cudaStream_t stream, int n_splits, float* part_o, float2* part_ml);
+                                  uint32_t* err, cudaStream_t stream, int n_splits, float* part_o, float2* part_ml,
+                                  int stop_after = -1);
 cudaError_t launch_attention_combine(const float* part_o, const float2* part_ml, uint16_t* out, int out_stride, int B,
                                      int T, int H, int n_splits, cudaStream_t stream);
 int attention_launches(int T, int n_splits);  // kernels one launch_attention makes (1 or 2)

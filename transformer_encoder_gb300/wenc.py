@@ -35,7 +35,7 @@ EXPORTED_SYMBOLS = (
     "wenc_version", "wenc_selftest_wait_timeout", "wenc_attention_static", "wenc_attention_static_capacity",
     "wenc_linear_tf32", "wenc_attention_tf32", "wenc_set_stem", "wenc_stem", "wenc_encode", "wenc_encode_launches",
     "wenc_set_cross_kv", "wenc_cross_kv", "wenc_selftest_gemm_schedule", "wenc_selftest_gemm_pair_abort",
-    "wenc_set_device_alloc_limit", "wenc_device_bytes_held",
+    "wenc_set_device_alloc_limit", "wenc_device_bytes_held", "wenc_selftest_attention_abort",
 )
 
 
@@ -96,6 +96,7 @@ def lib() -> ctypes.CDLL:
         L.wenc_sync_status.argtypes = [vp]
         L.wenc_selftest_wait_timeout.argtypes = [vp]
         L.wenc_selftest_gemm_pair_abort.argtypes = [vp, vp, vp, vp, i, i, i, i, vp]
+        L.wenc_selftest_attention_abort.argtypes = [vp, vp, vp, vp, i, i, i, i, vp]
         L.wenc_set_device_alloc_limit.argtypes = [ctypes.c_size_t]
         L.wenc_set_device_alloc_limit.restype = None
         L.wenc_device_bytes_held.argtypes = []
@@ -114,7 +115,7 @@ def lib() -> ctypes.CDLL:
                      "wenc_layernorm", "wenc_linear", "wenc_sync_status", "wenc_forward_launches",
                      "wenc_selftest_wait_timeout", "wenc_linear_tf32", "wenc_attention_tf32", "wenc_set_stem",
                      "wenc_stem", "wenc_encode", "wenc_encode_launches", "wenc_set_cross_kv", "wenc_cross_kv",
-                     "wenc_selftest_gemm_schedule", "wenc_selftest_gemm_pair_abort"):
+                     "wenc_selftest_gemm_schedule", "wenc_selftest_gemm_pair_abort", "wenc_selftest_attention_abort"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -394,6 +395,20 @@ def selftest_gemm_pair_abort(a, w, bias, stop_after: int, out=None, stream=None)
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
     _check(lib().wenc_selftest_gemm_pair_abort(_ptr(a), _ptr(w), _ptr(bias), _ptr(out), M, N, K, int(stop_after),
+                                              _stream(stream)))
+    return out
+
+
+def selftest_attention_abort(q, k, v, stop_after: int, out=None, stream=None):
+    """Launch the attention self-test (its producer stops after `stop_after` K tiles); returns the
+    (undefined) output; read the outcome with sync_status()."""
+    import torch
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _require(t, torch.bfloat16, n)
+    B, T, H, hd = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _check(lib().wenc_selftest_attention_abort(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, T, H, int(stop_after),
                                               _stream(stream)))
     return out
 
