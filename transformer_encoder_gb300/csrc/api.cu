@@ -12,12 +12,15 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cstdlib>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
 #include <string>
 #include <vector>
+
+#include <nvtx3/nvToolsExt.h>
 
 #include "launch.h"
 #include "ptx.cuh"
@@ -401,6 +404,30 @@ void enqueue_stem(wenc* h, const float* mel, float* x, int B, LaunchRec& rec) {
 }
 
 // The blocks first .. first+count-1 and, if final_ln, the final LayerNorm: in -> out.
+// Optional NVTX ranges (WENC_NVTX=1 in the environment): one range per block around its launches,
+// named "wenc block <l>", so that a profiler can select a block's kernels (for example with ncu's
+// --nvtx --nvtx-include "wenc block 5/"). Off by default: then no NVTX call is made.
+bool nvtx_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("WENC_NVTX");
+    return v && v[0] == '1';
+  }();
+  return on;
+}
+
+struct NvtxRange {
+  bool on;
+  explicit NvtxRange(int layer) : on(nvtx_enabled()) {
+    if (!on) return;
+    char name[32];
+    snprintf(name, sizeof(name), "wenc block %d", layer);
+    nvtxRangePushA(name);
+  }
+  ~NvtxRange() {
+    if (on) nvtxRangePop();
+  }
+};
+
 void enqueue_blocks(wenc* h, const float* in, float* out, int B, int first, int count, bool final_ln, LaunchRec& rec) {
   const wenc_config& c = h->cfg;
   const cudaStream_t s = rec.s;
@@ -410,6 +437,7 @@ void enqueue_blocks(wenc* h, const float* in, float* out, int B, int first, int 
   if (!h->tf32 && count > 0)  // statistics and bf16 copy of the first block's input
     rec(14, wenc_host::launch_row_stats(in, static_cast<uint16_t*>(h->xn), h->stats, M, d, h->seg_w, s));
   for (int l = first; l < first + count && rec.e == cudaSuccess; ++l) {
+    const NvtxRange range(l);
     const wenc::Layer& P = h->layers[l];
     const bool last = (l == first + count - 1);
     float* dst_final = (last && !final_ln) ? out : h->x;
