@@ -24,7 +24,9 @@
 //    traffic through shared memory) and rescale O in TMEM when the running maximum moves by more
 //    than 2^8. The two tiles take turns on the exponentials (ping-pong), so one tile's exps run
 //    while the other tile loads scores, stores P or waits, and the tensor pipe runs the other
-//    tile's products meanwhile. No T x T score buffer exists.
+//    tile's products meanwhile. The turn passes through hardware named barriers: a tile's warps
+//    resume a few tens of cycles after the other tile's arrive, where an mbarrier wait took
+//    ~115 (210 -> 197 us at T = 1500). No T x T score buffer exists.
 // The control warpgroup (warps 0-3) hands registers to the softmax warpgroups at start-up
 // (setmaxnreg: 104 and 200 per thread instead of 168 for all), which keeps a row's scores and the
 // exponential pipeline in registers (211.6 -> 197.5 us at large-v3 dims, B = 16; the four score
@@ -44,6 +46,14 @@ using namespace wenc_dev;
 
 // D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16 with bf16 operands; A = 128 lanes x 8 columns, each
 // 32-bit column holding two consecutive K elements (the lower one in the low half).
+// Hardware named barriers (ids 1 and 2; __syncthreads uses 0): `count` threads in whole warps.
+__device__ __forceinline__ void named_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_arrive(int id, int count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                              uint32_t accumulate) {
   asm volatile(
@@ -76,8 +86,9 @@ constexpr uint32_t OFF_K = OFF_Q + 4 * Q_BYTES;
 constexpr uint32_t OFF_V = OFF_K + NK * KV_BYTES;
 constexpr uint32_t OFF_BARS = OFF_V + NV * KV_BYTES;
 // bars: q_full[2], q_empty[2], k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], and per query
-// tile t: s_full[t], s_free[t], p_full[t], pv_done[t], turn[t]; drain
-constexpr int NUM_BARS = 4 + 2 * NK + 2 * NV + 10 + 1;
+// tile t: s_full[t], s_free[t], p_full[t], pv_done[t]; drain. (The exponential turn uses the
+// hardware named barriers 1 and 2.)
+constexpr int NUM_BARS = 4 + 2 * NK + 2 * NV + 8 + 1;
 constexpr size_t SMEM = 1024 + OFF_BARS + NUM_BARS * 8 + 16;
 constexpr uint32_t TMEM_COLS = 512;  // S_A 0..127, S_B 128..255, O_A 256..319, O_B 320..383, P_A 384..447, P_B 448..511
 // Grow the running maximum only when a tile's maximum exceeds it by more than this (log2
@@ -107,8 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto s_free = [&](int t) { return tb0 + 16u + 8u * t; };
   auto p_full = [&](int t) { return tb0 + 32u + 8u * t; };
   auto pv_done = [&](int t) { return tb0 + 48u + 8u * t; };
-  auto turn = [&](int t) { return tb0 + 64u + 8u * t; };  // tile t may run its exponentials
-  const uint32_t drain = tb0 + 80u;
+  const uint32_t drain = tb0 + 64u;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_BARS + NUM_BARS * 8);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   const WaitCtx wc{abort_flag, err};
@@ -155,7 +165,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(s_free(t), 4);  // one arrival per softmax warp of the tile
       mbar_init(p_full(t), 4);
       mbar_init(pv_done(t), 1);
-      mbar_init(turn(t), 4);  // the other tile's four softmax warps pass the turn
     }
     mbar_init(drain, 3);  // one commit per MMA-issuing thread
     *abort_flag = 0u;
@@ -301,8 +310,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    // The turn passes through two hardware named barriers of 256 threads: barrier 1 is tile A's
+    // turn, barrier 2 tile B's. The four warps taking the turn sync, the four passing it arrive.
+    // Per key tile, tile B syncs on 2 and arrives on 1; tile A syncs on 1 (from its second tile)
+    // and arrives on 2; tile A closes with one more sync on 1. Both tiles walk the same key tiles,
+    // so every phase completes. After a failed wait a warp runs the turn operations of the key
+    // tiles it has not walked yet before it stops, so the other tile never waits for it in vain.
     bool ok = true;
-    int g = 0;  // key tiles processed, across items
+    int g = 0;       // key tiles processed, across items
+    int g_turn = 0;  // the first key tile whose turn operations have not run
     for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
       const int kv0 = decode(w).kv0, n_kv = decode(w).n_kv;
       float m = -CUDART_INF_F;  // running maximum, in units of scale_log2
@@ -348,9 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Ping-pong: the two tiles take turns on the exponentials (MUFU), so that one tile's
         // exponentials overlap the other tile's loads, stores and waits instead of contending.
         // Tile A's turn j follows tile B's exponentials of tile j-1; tile B's follows A's of j.
-        if (t == 1 || g > 0) {
-          if (!mbar_wait_warp(turn(t), (t == 0 ? g - 1 : g) & 1, wc, 21)) { ok = false; break; }
-        }
+        if (t == 1 || g > 0) named_sync(1 + t, 256);
 
         // p = 2^(s * scale_log2 - m_new): packed fp32x2 FMA for the argument, packed adds for the
         // row sum; P is packed to bf16 pairs before waiting on the previous PV product.
@@ -372,7 +386,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         unpack_f32x2(sum2b, sb0, sb1);
         const float sum = (sa0 + sa1) + (sb0 + sb1);
         __syncwarp();
-        if (lane == 0) mbar_arrive(turn(1 - t));
+        named_arrive(2 - t, 256);  // the other tile's turn
+        g_turn = g + 1;
 
         if (j > 0) {
           // PV[j-1] must be complete: P is overwritten below and O may be rescaled.
@@ -411,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(p_full(t));
       }
       if (!ok) break;
-      if (!mbar_wait_warp(pv_done(t), (g - 1) & 1, wc, 19)) break;
+      if (!mbar_wait_warp(pv_done(t), (g - 1) & 1, wc, 19)) { ok = false; break; }
       {
         // The item's output, from O in TMEM once the PV product of its last key tile is done;
         // the next item's first PV product (which overwrites O) waits for P that this warp
@@ -458,6 +473,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    if (!ok) {
+      int n_tiles = 0;
+      for (int w = blockIdx.x; w < n_items; w += gridDim.x) n_tiles += decode(w).n_kv;
+      for (int gg = g_turn; gg < n_tiles; ++gg) {
+        if (t == 1 || gg > 0) named_sync(1 + t, 256);
+        named_arrive(2 - t, 256);
+      }
+    }
+    if (t == 0) named_sync(1, 256);  // tile B's last hand-over
   }
 
   tc_fence_before();
