@@ -624,6 +624,20 @@ def run_wenc(args, w):
     barrier()
     ms_e2e = e_start.elapsed_time(e_stop)
 
+    # The host link alone, outside the timed regions: one upload and one readback of a step's
+    # buffers on the copy stream (explains the part of e2e that the copies cannot overlap: the
+    # first upload and the last readback of the timed region).
+    def copy_ms(dst, src):
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(copy_stream):
+            c0.record(copy_stream)
+            dst.copy_(src, non_blocking=True)
+            c1.record(copy_stream)
+        torch.cuda.synchronize()
+        return c0.elapsed_time(c1)
+    h2d_ms = min(copy_ms(xs[0], x_host) for _ in range(3))
+    d2h_ms = min(copy_ms(outs_host[0], outs[0]) for _ in range(3))
+
     ms_total, ms_e2e = combine_rank_timings(ms_total, ms_e2e, world)
 
     ms_step = ms_total / args.steps
@@ -716,7 +730,8 @@ def run_wenc(args, w):
         "gpu_launches": n_launch * args.steps,
         "e2e": {"value": windows * args.steps / (ms_e2e / 1e3), "unit": "windows/s",
                 "h2d_bytes_per_step": x.numel() * 4, "d2h_bytes_per_step": out.numel() * 4,
-                "copies": "pinned host memory, on a copy stream overlapping the previous/next step (double-buffered)"},
+                "copies": "pinned host memory, on a copy stream overlapping the previous/next step (double-buffered)",
+                "h2d_gbs": x.numel() * 4 / (h2d_ms / 1e3) / 1e9, "d2h_gbs": out.numel() * 4 / (d2h_ms / 1e3) / 1e9},
         "clocks": clk,
     }
     enc.close()

@@ -40,6 +40,7 @@ def test_bench_line_keeps_the_contract():
     e = d["e2e"]
     assert e["unit"] == "windows/s" and e["value"] > 0
     assert e["h2d_bytes_per_step"] == e["d2h_bytes_per_step"] == 1500 * 384 * 4
+    assert e["h2d_gbs"] > 0 and e["d2h_gbs"] > 0
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(d["clocks"])
     pc = d["ms_per_step_pct"]
     assert pc["p10"] <= pc["p50"] <= pc["p90"] and abs(pc["p50"] - d["ms_per_step"]) < 0.5 * d["ms_per_step"]
